@@ -1,0 +1,251 @@
+/*
+ * kvattn.h -- C ABI of the RoPE + KV-cache + attention hot path of an LLM
+ * inference step, for one NVIDIA GB300 (sm_103a) GPU.
+ *
+ * The operations follow the problem statement of a set of web tutorials on
+ * hand-writing an LLM inference engine (cited per function below by page
+ * title and section):
+ *   [RoPE page]    "Hand-writing an LLM inference engine: Tokenizer, KV Cache
+ *                  and RoPE"
+ *   [Engine page]  "From-scratch AI inference engine: beyond calling packages"
+ *   [Nano-vLLM]    "Understanding an LLM inference engine through Nano-vLLM,
+ *                  Part 2"
+ *   [Series intro] "Hand-writing an LLM inference engine", chapter 1
+ *
+ * Conventions shared by every call
+ *   - Pointers documented "device" are CUDA device pointers owned by the
+ *     caller; the library never allocates, frees or retains device memory
+ *     (the one exception is a 4-byte module-scope device status word).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  GPU calls are asynchronous on that stream; a returned
+ *     KVATTN_OK means the work was validated and launched.
+ *   - Every argument the host can check is checked before anything is
+ *     launched; a failed check returns an error and launches nothing.
+ *   - Index errors only the GPU can see (a block id outside the pool, a
+ *     position past the block table) make the kernel skip that access and
+ *     record KVATTN_ERR_BAD_INDEX in the device status word; a bounded wait
+ *     that runs out records KVATTN_ERR_TIMEOUT.  Read and clear it with
+ *     kvattn_get_device_status().
+ *   - Element type: KVATTN_F32 or KVATTN_BF16 for q, k, v, the cache and the
+ *     output alike; arithmetic is fp32 with fp32 accumulation.
+ *   - Supported: head_dim 64 or 128, num_q_heads % num_kv_heads == 0 with
+ *     group size G = num_q_heads / num_kv_heads in {1, 2, 4, 8}.  Query head
+ *     j reads KV head j / G (contiguous groups).  Anything else returns
+ *     KVATTN_ERR_UNSUPPORTED.
+ *
+ * KV cache layout (one layer; K and V are separate pools):
+ *   k_pool, v_pool: [num_blocks][num_kv_heads][block_size][head_dim]
+ *   Token position p of the sequence owning block-table row r lives in block
+ *   b = block_table[r * max_blocks_per_seq + p / block_size] at offset
+ *   p % block_size ([Nano-vLLM], section 05: physical block from the table,
+ *   offset inside the block).  A paged cache uses block_size = 16; a
+ *   contiguous cache is the same layout with block_size = max_len and one
+ *   table column holding the row of each sequence ([Engine page],
+ *   section 3.2: contiguous per-sequence preallocation vs fixed-size pages).
+ *   block_size must be a multiple of 16 when max_blocks_per_seq > 1.
+ */
+#ifndef KVATTN_H
+#define KVATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVATTN_VERSION 1
+
+typedef enum {
+    KVATTN_OK = 0,
+    KVATTN_ERR_INVALID_ARG = 1,      /* null pointer, negative size, bad id ... */
+    KVATTN_ERR_UNSUPPORTED = 2,      /* head_dim / group size / dtype not built */
+    KVATTN_ERR_OUT_OF_BLOCKS = 3,    /* allocator exhausted (nothing allocated) */
+    KVATTN_ERR_WORKSPACE_TOO_SMALL = 4,
+    KVATTN_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+    KVATTN_ERR_TIMEOUT = 6,          /* device: a bounded wait ran out */
+    KVATTN_ERR_BAD_INDEX = 7         /* device: block id / position out of range */
+} kvattn_status;
+
+typedef enum { KVATTN_F32 = 0, KVATTN_BF16 = 1 } kvattn_dtype;
+
+typedef struct {
+    int32_t num_q_heads;   /* Hq */
+    int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0 */
+    int32_t head_dim;      /* D: 64 or 128 */
+    int32_t dtype;         /* kvattn_dtype */
+    float rope_base;       /* theta_i = rope_base^(-2i/D); 10000 on the pages */
+    float scale;           /* softmax scale; 0 => 1/sqrt(head_dim) */
+} kvattn_config;
+
+typedef struct {
+    void* k_pool;          /* device, [num_blocks][Hkv][block_size][D] */
+    void* v_pool;          /* device, same shape */
+    int64_t num_blocks;
+    int32_t block_size;
+} kvattn_cache;
+
+/* Library version (KVATTN_VERSION) and a static string for a status code. */
+int32_t kvattn_version(void);
+const char* kvattn_status_string(kvattn_status s);
+
+/*
+ * kvattn_rope_append -- rotary position embedding of the new tokens' q and k,
+ * fused with writing k (rotated) and v (as given) into the cache.
+ *
+ * [RoPE page], section 4: vector split into adjacent pairs (x0,x1),(x2,x3),...
+ * and pair i rotated by the 2-D rotation of angle m*theta_i,
+ * theta_i = rope_base^(-2i/D), m = the token's position:
+ *     x'[2i]   = x[2i] cos(m theta_i) - x[2i+1] sin(m theta_i)
+ *     x'[2i+1] = x[2i] sin(m theta_i) + x[2i+1] cos(m theta_i)
+ * [Engine page], section 3.2: the new token's K and V are written at the
+ * cache index equal to its absolute position, which is also the RoPE
+ * position.  v is not rotated ([Series intro], section 2.2: RoPE rotates Q
+ * and K).
+ *
+ *   q           device, [num_tokens][Hq][D], rotated IN PLACE
+ *   k, v        device, [num_tokens][Hkv][D], read only
+ *   positions   device, [num_tokens] int32, absolute position of each token
+ *   seq_ids     device, [num_tokens] int32, block-table row of each token
+ *   block_table device, [num_seqs][max_blocks_per_seq] int32
+ * Each stored element is the round-to-nearest-even of the rotation of the
+ * input values.  Tokens may belong to any rows, in any order; two tokens must
+ * not name the same (row, position).
+ * Errors: INVALID_ARG (null pointer, num_tokens < 0, num_seqs <= 0,
+ * bad cache), UNSUPPORTED, CUDA; device: BAD_INDEX (seq id, position or block
+ * out of range: that token is skipped).  num_tokens == 0 launches nothing.
+ */
+kvattn_status kvattn_rope_append(const kvattn_config* cfg, const kvattn_cache* cache, void* q,
+                                 const void* k, const void* v, const int32_t* positions,
+                                 const int32_t* seq_ids, const int32_t* block_table,
+                                 int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_tokens,
+                                 void* stream);
+
+/*
+ * Workspace bytes kvattn_decode needs for `batch` sequences of at most
+ * max_seq_len tokens with num_splits KV splits (0 = the library's choice for
+ * the current device; the same arguments give the same choice).
+ * Returns 0 for invalid arguments.
+ */
+size_t kvattn_decode_workspace_size(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len,
+                                    int32_t num_splits);
+
+/* The split count kvattn_decode uses for these arguments (num_splits=0 => auto). */
+int32_t kvattn_decode_num_splits(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len,
+                                 int32_t num_splits);
+
+/*
+ * kvattn_decode -- attention of one new query token per sequence against the
+ * whole cache of that sequence ([Engine page], section 3.3: with a KV cache
+ * the query length is 1 and the mask is (1, S), every cached key visible;
+ * section 3.1: softmax(q K^T / sqrt(d_k)) V with d_k = head_dim, scale
+ * applied before the softmax).
+ *
+ *   out[b][j] = sum_{i < seq_lens[b]} softmax_i(q[b][j] . K_b[i][j/G] * scale)
+ *               * V_b[i][j/G]
+ *
+ * The keys of a sequence are split into num_splits ranges processed in
+ * parallel, each producing a partial (max, sum, weighted V) that a second
+ * kernel merges with the online-softmax rescaling ([Engine page],
+ * section 3.4: running max m and running sum l, earlier results rescaled).
+ *
+ *   q           device, [batch][Hq][D] (already rotated)
+ *   block_table device, [batch][max_blocks_per_seq] int32; row b = sequence b
+ *   seq_lens    device, [batch] int32, tokens in the cache INCLUDING the new
+ *               one (call kvattn_rope_append first); 0 => out row is zeros
+ *   max_seq_len host upper bound of seq_lens (a larger length is a BAD_INDEX)
+ *   out         device, [batch][Hq][D]
+ *   workspace   device, >= kvattn_decode_workspace_size(...) bytes, any
+ *               contents, 256-byte aligned; not used after the call returns
+ *               except by the work it launched on `stream`.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA; device:
+ * BAD_INDEX, TIMEOUT.  batch == 0 launches nothing.
+ */
+kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                            int32_t num_splits, void* out, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * kvattn_prefill_chunk -- causal attention of chunks of new query tokens
+ * against their sequences' caches, which already hold the chunks' own keys
+ * (call kvattn_rope_append for the chunk tokens first).
+ * [Series intro], section 2.5 (prefill processes a whole prompt and fills the
+ * cache); [Engine page], section 3.3 (each position sees itself and earlier
+ * positions) and section 3.4 (tiled attention with an online softmax).
+ *
+ * Chunk c owns query rows cu_q_lens[c] .. cu_q_lens[c+1]-1 of q; row r of
+ * the chunk sits at absolute position prefix_lens[c] + r and sees keys
+ * 0 .. prefix_lens[c] + r of block-table row c.
+ *
+ *   q           device, [total_q][Hq][D] (already rotated), bf16 only
+ *   cu_q_lens   device, [num_chunks + 1] int32, cu_q_lens[0] = 0, non-decreasing
+ *   prefix_lens device, [num_chunks] int32
+ *   block_table device, [num_chunks][max_blocks_per_seq] int32
+ *   max_q_len   host upper bound of cu_q_lens[c+1] - cu_q_lens[c]
+ *   out         device, [total_q][Hq][D]
+ * Uses the tcgen05 tensor cores; needs block_size % 16 == 0 and
+ * head_dim == 128.  Errors: INVALID_ARG, UNSUPPORTED, CUDA; device:
+ * BAD_INDEX, TIMEOUT.  num_chunks == 0 launches nothing.
+ */
+kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache* cache,
+                                   const void* q, const int32_t* cu_q_lens,
+                                   const int32_t* prefix_lens, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, int32_t num_chunks,
+                                   int32_t max_q_len, int32_t total_q, void* out, void* stream);
+
+/*
+ * Waits for `stream`, then returns the device status word of the current
+ * device in *out (KVATTN_OK if no kernel recorded an error since the last
+ * read) and clears it.  Returns CUDA if the stream itself failed.
+ */
+kvattn_status kvattn_get_device_status(void* stream, int32_t* out);
+
+/*
+ * Host-side block allocator (the CPU "block manager" of [Nano-vLLM],
+ * section 05, and the page allocation of [RoPE page], section 5): a free
+ * list of fixed-size block ids 0 .. num_blocks-1 in host memory, with a
+ * reference count per block (a block shared by several sequences returns to
+ * the free list when its last reference is dropped).  Thread-safe.
+ */
+typedef struct kvattn_allocator kvattn_allocator;
+
+/* INVALID_ARG if num_blocks <= 0 or > 2^31-1 or out == NULL. */
+kvattn_status kvattn_allocator_create(int64_t num_blocks, kvattn_allocator** out);
+void kvattn_allocator_destroy(kvattn_allocator* a);
+
+/* Takes n free blocks (refcount 1) into out_ids, all or nothing: with fewer
+ * than n free it takes none, counts a failure and returns OUT_OF_BLOCKS. */
+kvattn_status kvattn_alloc_blocks(kvattn_allocator* a, int32_t n, int32_t* out_ids);
+
+/* Drops one reference of each id; validates all ids first (out of range or
+ * not allocated => INVALID_ARG and nothing changes; an id may appear at most
+ * as many times as it has references). */
+kvattn_status kvattn_free_blocks(kvattn_allocator* a, const int32_t* ids, int32_t n);
+
+/* Adds one reference to each (allocated) id: INVALID_ARG and nothing changes
+ * if one is not allocated. */
+kvattn_status kvattn_share_blocks(kvattn_allocator* a, const int32_t* ids, int32_t n);
+
+int64_t kvattn_allocator_num_free(const kvattn_allocator* a);
+int64_t kvattn_allocator_num_failures(const kvattn_allocator* a);
+int32_t kvattn_allocator_refcount(const kvattn_allocator* a, int32_t id); /* -1 if out of range */
+
+/*
+ * Grows one sequence's host block-table row from cur_len to new_len tokens:
+ * allocates the blocks for positions cur_len .. new_len-1 that are not yet
+ * covered and writes their ids into table_row[cur blocks ...].  All or
+ * nothing.  INVALID_ARG if new_len < cur_len or the row is too narrow.
+ */
+kvattn_status kvattn_table_grow(kvattn_allocator* a, int32_t* table_row, int32_t max_blocks,
+                                int32_t block_size, int32_t cur_len, int32_t new_len);
+
+/* Frees the blocks covering a sequence of len tokens and sets those entries to -1. */
+kvattn_status kvattn_table_release(kvattn_allocator* a, int32_t* table_row, int32_t max_blocks,
+                                   int32_t block_size, int32_t len);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVATTN_H */

@@ -1,0 +1,302 @@
+"""Python binding of kvattn, the GB300 (sm_103a) RoPE + KV-cache + attention library.
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libkvattn.so`` (built from ``csrc/`` by ``build()``), reached through the C
+ABI declared in ``include/kvattn.h``.  PyTorch supplies device memory and the
+current stream.  There is no CPU fallback: importing this package without the
+built library raises, and every call raises ``KvattnError`` on a non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+F32 = 0
+BF16 = 1
+
+STATUS = {
+    0: "KVATTN_OK",
+    1: "KVATTN_ERR_INVALID_ARG",
+    2: "KVATTN_ERR_UNSUPPORTED",
+    3: "KVATTN_ERR_OUT_OF_BLOCKS",
+    4: "KVATTN_ERR_WORKSPACE_TOO_SMALL",
+    5: "KVATTN_ERR_CUDA",
+    6: "KVATTN_ERR_TIMEOUT",
+    7: "KVATTN_ERR_BAD_INDEX",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+EXPORTED = [
+    "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_decode_workspace_size",
+    "kvattn_decode_num_splits", "kvattn_decode", "kvattn_prefill_chunk", "kvattn_get_device_status",
+    "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
+    "kvattn_share_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
+    "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
+]
+
+
+class KvattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = int(code)
+        self.name = STATUS.get(self.code, f"status {code}")
+        super().__init__(f"{what}: {self.name}")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("rope_base", ctypes.c_float), ("scale", ctypes.c_float)]
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"kvattn CUDA library not built ({LIB_PATH} missing): run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    i32, i64, p, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    cfgp, cachep = ctypes.POINTER(Config), ctypes.POINTER(CacheDesc)
+    sig = {
+        "kvattn_version": ([], i32),
+        "kvattn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "kvattn_rope_append": ([cfgp, cachep, p, p, p, p, p, p, i32, i32, i32, p], ctypes.c_int),
+        "kvattn_decode_workspace_size": ([cfgp, i32, i32, i32], sz),
+        "kvattn_decode_num_splits": ([cfgp, i32, i32, i32], i32),
+        "kvattn_decode": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p, sz, p], ctypes.c_int),
+        "kvattn_prefill_chunk": ([cfgp, cachep, p, p, p, p, i32, i32, i32, i32, p, p], ctypes.c_int),
+        "kvattn_get_device_status": ([p, ctypes.POINTER(i32)], ctypes.c_int),
+        "kvattn_allocator_create": ([i64, ctypes.POINTER(p)], ctypes.c_int),
+        "kvattn_allocator_destroy": ([p], None),
+        "kvattn_alloc_blocks": ([p, i32, p], ctypes.c_int),
+        "kvattn_free_blocks": ([p, p, i32], ctypes.c_int),
+        "kvattn_share_blocks": ([p, p, i32], ctypes.c_int),
+        "kvattn_allocator_num_free": ([p], i64),
+        "kvattn_allocator_num_failures": ([p], i64),
+        "kvattn_allocator_refcount": ([p, i32], i32),
+        "kvattn_table_grow": ([p, p, i32, i32, i32, i32], ctypes.c_int),
+        "kvattn_table_release": ([p, p, i32, i32, i32], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def check(code: int, what: str) -> None:
+    if code != 0:
+        raise KvattnError(code, what)
+
+
+def version() -> int:
+    return int(lib.kvattn_version())
+
+
+def status_string(code: int) -> str:
+    return lib.kvattn_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------------------ torch-facing helpers
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def make_config(num_q_heads: int, num_kv_heads: int, head_dim: int, dtype: int,
+                rope_base: float = 10000.0, scale: float = 0.0) -> Config:
+    return Config(num_q_heads, num_kv_heads, head_dim, dtype, rope_base, scale)
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _dev(t, name: str, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Cache:
+    """One layer's K and V pools, [num_blocks, Hkv, block_size, D] each (device tensors, caller-owned)."""
+
+    def __init__(self, k_pool, v_pool):
+        if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+            raise ValueError("k_pool and v_pool must both be [num_blocks, Hkv, block_size, D]")
+        self.k_pool, self.v_pool = k_pool, v_pool
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k_pool.shape
+        self.desc = CacheDesc(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool", k_pool.dtype),
+                              int(self.num_blocks), int(self.block_size))
+
+    @classmethod
+    def empty(cls, num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int, dtype, device="cuda"):
+        torch = _torch()
+        k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=dtype, device=device)
+        v = torch.empty_like(k)
+        return cls(k, v)
+
+
+def rope_append(cfg: Config, cache: Cache, q, k, v, positions, seq_ids, block_table, stream=None) -> None:
+    """kvattn_rope_append: rotate q in place, write rotated k and raw v into the cache."""
+    torch = _torch()
+    T = q.shape[0]
+    check(lib.kvattn_rope_append(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q"),
+                                 _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
+                                 _dev(positions, "positions", torch.int32),
+                                 _dev(seq_ids, "seq_ids", torch.int32),
+                                 _dev(block_table, "block_table", torch.int32),
+                                 block_table.shape[0], block_table.shape[1], T, _stream(stream)),
+          "kvattn_rope_append")
+
+
+def decode_workspace_size(cfg: Config, batch: int, max_seq_len: int, num_splits: int = 0) -> int:
+    return int(lib.kvattn_decode_workspace_size(ctypes.byref(cfg), batch, max_seq_len, num_splits))
+
+
+def decode_num_splits(cfg: Config, batch: int, max_seq_len: int, num_splits: int = 0) -> int:
+    return int(lib.kvattn_decode_num_splits(ctypes.byref(cfg), batch, max_seq_len, num_splits))
+
+
+def decode(cfg: Config, cache: Cache, q, block_table, seq_lens, max_seq_len: int, out=None,
+           workspace=None, num_splits: int = 0, stream=None):
+    """kvattn_decode: one query token per sequence against its whole cache."""
+    torch = _torch()
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = decode_workspace_size(cfg, B, max_seq_len, num_splits)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    check(lib.kvattn_decode(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q"),
+                            _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+                            _dev(seq_lens, "seq_lens", torch.int32), B, int(max_seq_len), int(num_splits),
+                            _dev(out, "out", q.dtype), _dev(workspace, "workspace"), workspace.numel(),
+                            _stream(stream)),
+          "kvattn_decode")
+    return out
+
+
+def prefill_chunk(cfg: Config, cache: Cache, q, cu_q_lens, prefix_lens, block_table, max_q_len: int,
+                  out=None, stream=None):
+    """kvattn_prefill_chunk: causal attention of query chunks over their caches."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    check(lib.kvattn_prefill_chunk(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q"),
+                                   _dev(cu_q_lens, "cu_q_lens", torch.int32),
+                                   _dev(prefix_lens, "prefix_lens", torch.int32),
+                                   _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+                                   prefix_lens.shape[0], int(max_q_len), q.shape[0],
+                                   _dev(out, "out", q.dtype), _stream(stream)),
+          "kvattn_prefill_chunk")
+    return out
+
+
+def get_device_status(stream=None) -> int:
+    """Waits for the stream and returns (and clears) the device status word."""
+    v = ctypes.c_int32(0)
+    check(lib.kvattn_get_device_status(_stream(stream), ctypes.byref(v)), "kvattn_get_device_status")
+    return int(v.value)
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)
+
+
+# ------------------------------------------------------------------ host allocator
+
+class BlockAllocator:
+    """Host free list of KV block ids with reference counts (C++, thread-safe)."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        check(lib.kvattn_allocator_create(int(num_blocks), ctypes.byref(h)), "kvattn_allocator_create")
+        self._h = h
+        self.num_blocks = int(num_blocks)
+
+    def close(self) -> None:
+        if self._h:
+            lib.kvattn_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int):
+        import numpy as np
+
+        out = np.empty(int(n), dtype=np.int32)
+        check(lib.kvattn_alloc_blocks(self._h, int(n), out.ctypes.data_as(ctypes.c_void_p)), "kvattn_alloc_blocks")
+        return out
+
+    def free(self, ids) -> None:
+        import numpy as np
+
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        check(lib.kvattn_free_blocks(self._h, a.ctypes.data_as(ctypes.c_void_p), a.size), "kvattn_free_blocks")
+
+    def share(self, ids) -> None:
+        import numpy as np
+
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        check(lib.kvattn_share_blocks(self._h, a.ctypes.data_as(ctypes.c_void_p), a.size), "kvattn_share_blocks")
+
+    def grow(self, table_row, block_size: int, cur_len: int, new_len: int) -> None:
+        """Allocates blocks so the int32 numpy row covers new_len tokens (in place)."""
+        if table_row.dtype.name != "int32" or not table_row.flags.c_contiguous:
+            raise TypeError("table_row must be a contiguous int32 numpy array")
+        check(lib.kvattn_table_grow(self._h, table_row.ctypes.data_as(ctypes.c_void_p), table_row.size,
+                                    int(block_size), int(cur_len), int(new_len)), "kvattn_table_grow")
+
+    def release(self, table_row, block_size: int, length: int) -> None:
+        if table_row.dtype.name != "int32" or not table_row.flags.c_contiguous:
+            raise TypeError("table_row must be a contiguous int32 numpy array")
+        check(lib.kvattn_table_release(self._h, table_row.ctypes.data_as(ctypes.c_void_p), table_row.size,
+                                       int(block_size), int(length)), "kvattn_table_release")
+
+    @property
+    def num_free(self) -> int:
+        return int(lib.kvattn_allocator_num_free(self._h))
+
+    @property
+    def num_failures(self) -> int:
+        return int(lib.kvattn_allocator_num_failures(self._h))
+
+    def refcount(self, block_id: int) -> int:
+        return int(lib.kvattn_allocator_refcount(self._h, int(block_id)))

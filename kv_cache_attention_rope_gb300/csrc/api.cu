@@ -1,0 +1,308 @@
+// C ABI of kvattn: argument validation, per-device set-up, dispatch to the
+// kernels.  Every check the host can make is made here, before any launch.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kvattn_internal.cuh"
+
+namespace kvattn {
+
+// Module-scope device status word: first device-side error since the last
+// kvattn_get_device_status().  One instance per device that loads the module.
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+}  // namespace
+
+int* device_status_ptr()
+{
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int num_sms()
+{
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+namespace {
+
+bool config_ok(const kvattn_config* c)
+{
+    return c && c->num_q_heads > 0 && c->num_kv_heads > 0 && c->head_dim > 0 &&
+           (c->dtype == KVATTN_F32 || c->dtype == KVATTN_BF16) && std::isfinite(c->rope_base) &&
+           c->rope_base > 0.f && std::isfinite(c->scale) && c->scale >= 0.f;
+}
+
+kvattn_status config_supported(const kvattn_config* c)
+{
+    if (c->num_q_heads % c->num_kv_heads != 0) return KVATTN_ERR_UNSUPPORTED;
+    const int g = c->num_q_heads / c->num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return KVATTN_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128) return KVATTN_ERR_UNSUPPORTED;
+    return KVATTN_OK;
+}
+
+bool cache_ok(const kvattn_cache* k, int32_t max_blocks_per_seq)
+{
+    if (!k || !k->k_pool || !k->v_pool || k->num_blocks <= 0 || k->num_blocks > INT32_MAX || k->block_size <= 0)
+        return false;
+    if (max_blocks_per_seq <= 0) return false;
+    // a 16-token tile must not cross a block boundary
+    if (max_blocks_per_seq > 1 && k->block_size % 16 != 0) return false;
+    // 16-byte alignment of the pools (bulk copies)
+    if ((reinterpret_cast<uintptr_t>(k->k_pool) | reinterpret_cast<uintptr_t>(k->v_pool)) & 15u) return false;
+    return true;
+}
+
+float scale_of(const kvattn_config* c)
+{
+    return c->scale > 0.f ? c->scale : 1.0f / std::sqrt((float)c->head_dim);
+}
+
+// Host tables of the rotary embedding for (base, D): per-pair speed in 2^-64
+// turns per position, and the float-float cos/sin of k*pi/16, k = 0..4, from
+// their nested-radical closed forms (exactly rounded square roots, so the
+// values do not depend on the host's libm).
+void rope_tables(double base, int d, RopeArgs& a)
+{
+    static thread_local double cached_base = -1.0;
+    static thread_local int cached_d = -1;
+    static thread_local uint64_t turns[64];
+    if (cached_base != base || cached_d != d) {
+        const double two_pi = 6.283185307179586476925286766559;
+        for (int i = 0; i < d / 2; ++i) {
+            const double f = std::pow(base, -2.0 * (double)i / (double)d) / two_pi;  // turns per position
+            turns[i] = (uint64_t)std::llrint(std::ldexp(f, 64));  // f < 1/(2 pi): fits in int64
+        }
+        cached_base = base;
+        cached_d = d;
+    }
+    std::memcpy(a.turns, turns, sizeof(turns));
+    const double r2 = std::sqrt(2.0);
+    const double c[5] = {1.0, 0.5 * std::sqrt(2.0 + std::sqrt(2.0 + r2)), 0.5 * std::sqrt(2.0 + r2),
+                         0.5 * std::sqrt(2.0 + std::sqrt(2.0 - r2)), 0.5 * r2};
+    const double s[5] = {0.0, 0.5 * std::sqrt(2.0 - std::sqrt(2.0 + r2)), 0.5 * std::sqrt(2.0 - r2),
+                         0.5 * std::sqrt(2.0 - std::sqrt(2.0 - r2)), 0.5 * r2};
+    for (int k = 0; k < 5; ++k) {
+        const float ch = (float)c[k], sh = (float)s[k];
+        a.sector[k] = make_float4(ch, (float)(c[k] - (double)ch), sh, (float)(s[k] - (double)sh));
+    }
+}
+
+}  // namespace
+}  // namespace kvattn
+
+using namespace kvattn;
+
+extern "C" {
+
+int32_t kvattn_version(void) { return KVATTN_VERSION; }
+
+const char* kvattn_status_string(kvattn_status s)
+{
+    switch (s) {
+        case KVATTN_OK: return "ok";
+        case KVATTN_ERR_INVALID_ARG: return "invalid argument";
+        case KVATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KVATTN_ERR_OUT_OF_BLOCKS: return "out of KV blocks";
+        case KVATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case KVATTN_ERR_CUDA: return "CUDA error";
+        case KVATTN_ERR_TIMEOUT: return "device wait timed out";
+        case KVATTN_ERR_BAD_INDEX: return "block id or position out of range";
+    }
+    return "unknown status";
+}
+
+kvattn_status kvattn_rope_append(const kvattn_config* cfg, const kvattn_cache* cache, void* q, const void* k,
+                                 const void* v, const int32_t* positions, const int32_t* seq_ids,
+                                 const int32_t* block_table, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                 int32_t num_tokens, void* stream)
+{
+    if (!config_ok(cfg) || num_tokens < 0 || num_seqs <= 0) return KVATTN_ERR_INVALID_ARG;
+    kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
+    if (num_tokens == 0) return KVATTN_OK;
+    if (!q || !k || !v || !positions || !seq_ids || !block_table) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+        return KVATTN_ERR_INVALID_ARG;
+    RopeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.k_pool = cache->k_pool;
+    a.v_pool = cache->v_pool;
+    a.positions = positions;
+    a.seq_ids = seq_ids;
+    a.block_table = block_table;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = cache->block_size;
+    a.num_seqs = num_seqs;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_tokens = num_tokens;
+    a.hq = cfg->num_q_heads;
+    a.hkv = cfg->num_kv_heads;
+    a.d = cfg->head_dim;
+    a.dtype = cfg->dtype;
+    a.status = device_status_ptr();
+    if (!a.status) return KVATTN_ERR_CUDA;
+    rope_tables((double)cfg->rope_base, cfg->head_dim, a);
+    return launch_rope_append(a, static_cast<cudaStream_t>(stream));
+}
+
+int32_t kvattn_decode_num_splits(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len, int32_t num_splits)
+{
+    if (!config_ok(cfg) || config_supported(cfg) != KVATTN_OK || batch < 0 || max_seq_len < 0 || num_splits < 0)
+        return 0;
+    const DecodePlan p = decode_plan(batch, cfg->num_kv_heads, cfg->num_q_heads / cfg->num_kv_heads,
+                                     max_seq_len, num_splits);
+    return p.max_chunks;
+}
+
+size_t kvattn_decode_workspace_size(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len,
+                                    int32_t num_splits)
+{
+    const int32_t chunks = kvattn_decode_num_splits(cfg, batch, max_seq_len, num_splits);
+    if (chunks <= 0) return 0;
+    const size_t rows = (size_t)batch * cfg->num_q_heads * chunks;
+    const size_t o_bytes = (rows * cfg->head_dim * 4 + 255) / 256 * 256;
+    const size_t ml_bytes = (rows * 2 * 4 + 255) / 256 * 256;
+    return std::max<size_t>(256, o_bytes + ml_bytes);
+}
+
+kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,
+                            const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream)
+{
+    if (!config_ok(cfg) || batch < 0 || max_seq_len < 0 || num_splits < 0) return KVATTN_ERR_INVALID_ARG;
+    kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
+    if (batch == 0) return KVATTN_OK;
+    if (batch > 8192) return KVATTN_ERR_UNSUPPORTED;
+    if (!q || !block_table || !seq_lens || !out) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return KVATTN_ERR_INVALID_ARG;
+    const size_t need = kvattn_decode_workspace_size(cfg, batch, max_seq_len, num_splits);
+    if (need == 0) return KVATTN_ERR_INVALID_ARG;
+    const DecodePlan p = decode_plan(batch, cfg->num_kv_heads, cfg->num_q_heads / cfg->num_kv_heads, max_seq_len,
+                                     num_splits);
+    if (p.max_chunks > 1) {
+        if (!workspace || workspace_bytes < need) return KVATTN_ERR_WORKSPACE_TOO_SMALL;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return KVATTN_ERR_INVALID_ARG;
+    }
+    DecodeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k_pool = cache->k_pool;
+    a.v_pool = cache->v_pool;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    const size_t rows = (size_t)batch * cfg->num_q_heads * p.max_chunks;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                     (rows * cfg->head_dim * 4 + 255) / 256 * 256)
+                          : nullptr;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = cache->block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.batch = batch;
+    a.max_seq_len = max_seq_len;
+    a.splits = p.max_chunks;
+    a.chunk_tiles = p.chunk_tiles;
+    a.hq = cfg->num_q_heads;
+    a.hkv = cfg->num_kv_heads;
+    a.d = cfg->head_dim;
+    a.dtype = cfg->dtype;
+    a.scale_log2 = scale_of(cfg) * 1.4426950408889634f;
+    a.status = device_status_ptr();
+    if (!a.status) return KVATTN_ERR_CUDA;
+    return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,
+                                   const int32_t* cu_q_lens, const int32_t* prefix_lens,
+                                   const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_chunks,
+                                   int32_t max_q_len, int32_t total_q, void* out, void* stream)
+{
+    if (!config_ok(cfg) || num_chunks < 0 || max_q_len < 0 || total_q < 0) return KVATTN_ERR_INVALID_ARG;
+    kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128) return KVATTN_ERR_UNSUPPORTED;
+    if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
+    if (cache->block_size % 16 != 0) return KVATTN_ERR_UNSUPPORTED;
+    if (num_chunks == 0 || total_q == 0) return KVATTN_OK;
+    if (!q || !cu_q_lens || !prefix_lens || !block_table || !out) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return KVATTN_ERR_INVALID_ARG;
+    PrefillArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k_pool = cache->k_pool;
+    a.v_pool = cache->v_pool;
+    a.cu_q_lens = cu_q_lens;
+    a.prefix_lens = prefix_lens;
+    a.block_table = block_table;
+    a.out = out;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = cache->block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_chunks = num_chunks;
+    a.max_q_len = max_q_len;
+    a.total_q = total_q;
+    a.hq = cfg->num_q_heads;
+    a.hkv = cfg->num_kv_heads;
+    a.d = cfg->head_dim;
+    a.scale_log2 = scale_of(cfg) * 1.4426950408889634f;
+    a.status = device_status_ptr();
+    if (!a.status) return KVATTN_ERR_CUDA;
+    return launch_prefill(a, static_cast<cudaStream_t>(stream));
+}
+
+kvattn_status kvattn_get_device_status(void* stream, int32_t* out)
+{
+    if (!out) return KVATTN_ERR_INVALID_ARG;
+    int* p = device_status_ptr();
+    if (!p) return KVATTN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVATTN_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KVATTN_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return KVATTN_ERR_CUDA;
+    *out = v;
+    return KVATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+// Internal declarations shared by the kvattn CUDA translation units:
+// launch entry points, device status reporting, and thin inline-PTX wrappers
+// for the sm_100-family asynchronous machinery (mbarrier, bulk copies,
+// tcgen05).  Everything here is written from the public PTX ISA description.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvattn.h"
+
+namespace kvattn {
+
+// ---------------------------------------------------------------- host side
+
+// Device status word of the current device (a module-scope __device__ int).
+int* device_status_ptr();
+
+// One-line CUDA error mapping.
+inline kvattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA; }
+
+int num_sms();
+
+struct RopeArgs {
+    void* q;
+    const void* k;
+    const void* v;
+    void* k_pool;
+    void* v_pool;
+    const int32_t* positions;
+    const int32_t* seq_ids;
+    const int32_t* block_table;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_seqs;
+    int32_t max_blocks;
+    int32_t num_tokens;
+    int32_t hq, hkv, d;
+    int32_t dtype;
+    int* status;
+    // per-pair rotation speed in turns per position, 2^-64 fixed point:
+    // round(base^(-2i/D) / (2 pi) * 2^64)
+    uint64_t turns[64];
+    // cos/sin of k*pi/16, k = 0..4, as float-float pairs (c_hi, c_lo, s_hi, s_lo)
+    float4 sector[5];
+};
+kvattn_status launch_rope_append(const RopeArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    void* out;
+    float* part_o;     // [batch][hq][splits][d]
+    float* part_ml;    // [batch][hq][splits][2] (max in log2 units, sum)
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t max_blocks;
+    int32_t batch;
+    int32_t max_seq_len;
+    int32_t splits;       // partial slots per (sequence, head) = plan.max_chunks
+    int32_t chunk_tiles;  // 16-token tiles per chunk
+    int32_t hq, hkv, d;
+    int32_t dtype;
+    float scale_log2;  // softmax scale * log2(e)
+    int* status;
+};
+kvattn_status launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// How the keys of each sequence are cut into chunks: chunks of chunk_tiles
+// 16-token tiles, at most max_chunks per sequence.  splits > 0 asks for at
+// most `splits` chunks of the longest sequence; 0 lets the library choose.
+struct DecodePlan {
+    int32_t chunk_tiles;
+    int32_t max_chunks;
+};
+DecodePlan decode_plan(int32_t batch, int32_t hkv, int32_t group, int32_t max_seq_len, int32_t splits);
+
+struct PrefillArgs {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* cu_q_lens;
+    const int32_t* prefix_lens;
+    const int32_t* block_table;
+    void* out;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t max_blocks;
+    int32_t num_chunks;
+    int32_t max_q_len;
+    int32_t total_q;
+    int32_t hq, hkv, d;
+    float scale_log2;
+    int* status;
+};
+kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- device side
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void record_error(int* status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// mbarrier (shared::cta) --------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait limit of every bounded wait: a legitimate wait here is microseconds.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Bounded phase wait.  Returns false (and records KVATTN_ERR_TIMEOUT) if the
+// phase with the given parity has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(status, KVATTN_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bulk (non-tensor) asynchronous copy global -> shared, completion counted
+// in bytes on `bar`.  Both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read once (streamed KV pages).
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bf16 <-> fp32 on raw bits -----------------------------------------------
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace kvattn

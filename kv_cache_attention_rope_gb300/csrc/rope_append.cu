@@ -1,0 +1,276 @@
+// Fused rotary position embedding + KV-cache append.
+//
+// "Tokenizer, KV Cache and RoPE" page, section 4: adjacent pairs (x[2i],
+// x[2i+1]) of a query/key head vector rotate by m*theta_i, theta_i =
+// base^(-2i/D), m = the token position.  "From-scratch AI inference engine"
+// page, section 3.2: the new token's K/V go to the cache index equal to that
+// same position.  One CTA per token: it rotates every q head in place, rotates
+// every k head into the cache slot and copies v into the cache slot, moving
+// 16-byte vectors (8 bf16 / 4 fp32 values).
+//
+// Rounding.  A stored element is round-to-nearest-even of the exact rotation
+// of the input values.  The angle is reduced exactly: the rotation speed of
+// pair i is held as a 64-bit fixed-point count of turns per position
+// (round(theta_i / 2pi * 2^64)), so position * speed mod 2^64 is the angle's
+// fraction of a turn with no cancellation at large positions.  Fast path:
+// sincospif of that fraction and one fp32 fma per output, with a rigorous
+// error bound delta = 2^-20 (|x0| + |x1|); if both ends of [y - delta,
+// y + delta] round to the same bf16 value that value is the correctly rounded
+// result.  Otherwise (a fraction of a percent of the elements, mostly results
+// near zero or near a rounding boundary) the element is recomputed in
+// float-float arithmetic (about 44 bits) with a twiddle from quadrant and
+// 1/32-turn sector reduction plus short Taylor series.  fp32 outputs always
+// take the float-float path.
+#include "kvattn_internal.cuh"
+
+namespace kvattn {
+namespace {
+
+// ---------------------------------------------------------- float-float
+
+struct ff {
+    float hi, lo;
+};
+
+__device__ __forceinline__ ff two_sum(float a, float b)
+{
+    float s = __fadd_rn(a, b);
+    float bb = __fsub_rn(s, a);
+    float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
+}
+
+__device__ __forceinline__ ff fast_two_sum(float a, float b)  // needs |a| >= |b| or a == 0
+{
+    float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ ff two_prod(float a, float b)
+{
+    float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ ff ff_mul(ff x, ff y)
+{
+    ff p = two_prod(x.hi, y.hi);
+    float t = __fmaf_rn(x.hi, y.lo, __fmul_rn(x.lo, y.hi));
+    return fast_two_sum(p.hi, __fadd_rn(p.lo, t));
+}
+
+__device__ __forceinline__ ff ff_mul_f(ff x, float y)
+{
+    ff p = two_prod(x.hi, y);
+    return fast_two_sum(p.hi, __fmaf_rn(x.lo, y, p.lo));
+}
+
+__device__ __forceinline__ ff ff_add(ff x, ff y)
+{
+    ff s = two_sum(x.hi, y.hi);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+
+__device__ __forceinline__ ff ff_add_f(ff x, float y)
+{
+    ff s = two_sum(x.hi, y);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, x.lo));
+}
+
+__device__ __forceinline__ ff ff_neg(ff x) { return {-x.hi, -x.lo}; }
+
+// 2*pi split into float + float (the tail is 2*pi - float(2*pi)).
+constexpr float kTwoPiHi = 6.28318548202514648f;
+constexpr float kTwoPiLo = -1.7484555314695172e-07f;
+
+// 1/n! split into float + float (host-side double rounding of exact rationals).
+struct ffc {
+    float hi, lo;
+};
+__host__ __device__ constexpr ffc make_ffc(double d) { return {(float)d, (float)(d - (double)(float)d)}; }
+
+// Accurate (cos, sin) of the angle u * 2^-64 turns.
+// Quadrant reduction (exact swap/negate), then the nearest 1/32 turn k*pi/16
+// with |k| <= 4 from a 5-entry float-float table of nested-radical values,
+// then Taylor series of the remainder x (|x| <= pi/32): terms above ~1e-6 in
+// float-float, the rest in float.  Absolute error about 2^-44.
+__device__ __noinline__ void accurate_twiddle(uint64_t u, const float4* sector, ff& c_out, ff& s_out)
+{
+    const uint32_t quad = (uint32_t)((u + (1ull << 61)) >> 62);  // nearest quarter turn
+    const int64_t rs = (int64_t)(u - ((uint64_t)quad << 62));     // [-2^61, 2^61)
+    const int32_t k = (int32_t)((rs + (1ll << 58)) >> 59);        // nearest 1/32 turn, [-4, 4]
+    const int64_t r = rs - ((int64_t)k << 59);                    // [-2^58, 2^58]
+    const float r_hi = (float)r;
+    const float r_lo = (float)(r - (int64_t)r_hi);
+    const ff x = ff_mul({r_hi * 0x1p-64f, r_lo * 0x1p-64f}, {kTwoPiHi, kTwoPiLo});
+    const ff x2 = ff_mul(x, x);
+    const float t = x2.hi;
+
+    constexpr ffc c2 = make_ffc(-1.0 / 2.0), c4 = make_ffc(1.0 / 24.0);
+    constexpr ffc s3 = make_ffc(-1.0 / 6.0);
+    // cos x = 1 + x2*(-1/2 + x2*(1/24 + x2*(-1/720 + x2/40320)))
+    const float ctail = t * (-1.0f / 720.0f + t * (1.0f / 40320.0f));
+    ff cpoly = ff_add_f({c4.hi, c4.lo}, ctail);
+    cpoly = ff_add(ff{c2.hi, c2.lo}, ff_mul(x2, cpoly));
+    const ff cx = ff_add_f(ff_mul(x2, cpoly), 1.0f);
+    // sin x = x + x*x2*(-1/6 + x2*(1/120 - x2/5040))
+    const float stail = t * (1.0f / 120.0f - t * (1.0f / 5040.0f));
+    const ff spoly = ff_add_f({s3.hi, s3.lo}, stail);
+    const ff sx = ff_add(x, ff_mul(ff_mul(x, x2), spoly));
+
+    const float4 e = sector[k < 0 ? -k : k];
+    const ff ck = {e.x, e.y};
+    const ff sk = k < 0 ? ff{-e.z, -e.w} : ff{e.z, e.w};
+    // angle a_k + x
+    const ff ca = ff_add(ff_mul(ck, cx), ff_neg(ff_mul(sk, sx)));
+    const ff sa = ff_add(ff_mul(sk, cx), ff_mul(ck, sx));
+    switch (quad & 3u) {
+        case 0: c_out = ca; s_out = sa; break;
+        case 1: c_out = ff_neg(sa); s_out = ca; break;
+        case 2: c_out = ff_neg(ca); s_out = ff_neg(sa); break;
+        default: c_out = sa; s_out = ff_neg(ca); break;
+    }
+}
+
+// Round-to-nearest-even of the float-float value y to bf16 bits.
+__device__ __forceinline__ uint32_t rne_bf16_ff(ff y)
+{
+    const uint32_t b = __float_as_uint(y.hi);
+    if ((b & 0xffffu) == 0x8000u && y.lo != 0.0f) {
+        // y.hi sits exactly on a bf16 rounding boundary: the tail decides
+        const bool away = (y.lo > 0.0f) == (y.hi > 0.0f);
+        return ((b & 0xffff0000u) + (away ? 0x10000u : 0u)) >> 16;
+    }
+    __nv_bfloat16 h = __float2bfloat16_rn(y.hi);
+    return (uint32_t)(*reinterpret_cast<uint16_t*>(&h));
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x)
+{
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return (uint32_t)(*reinterpret_cast<uint16_t*>(&h));
+}
+
+// Accurate rotation of one pair with the float-float twiddle.
+__device__ __forceinline__ void rotate_pair_ff(float x0, float x1, uint64_t u, const float4* sector, ff& y0,
+                                               ff& y1)
+{
+    ff c, s;
+    accurate_twiddle(u, sector, c, s);
+    y0 = ff_add(ff_mul_f(c, x0), ff_neg(ff_mul_f(s, x1)));
+    y1 = ff_add(ff_mul_f(s, x0), ff_mul_f(c, x1));
+}
+
+// Rotates the bf16 pair packed in `w` (low half = even element).
+__device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, float2 cs, uint64_t u, const float4* sector)
+{
+    const float x0 = bf16lo(w), x1 = bf16hi(w);
+    const float y0 = __fmaf_rn(x0, cs.x, -__fmul_rn(x1, cs.y));
+    const float y1 = __fmaf_rn(x0, cs.y, __fmul_rn(x1, cs.x));
+    const float delta = 0x1p-20f * (fabsf(x0) + fabsf(x1));
+    uint32_t b0 = bf16_bits(y0), b1 = bf16_bits(y1);
+    const bool safe = bf16_bits(y0 - delta) == b0 && bf16_bits(y0 + delta) == b0 &&
+                      bf16_bits(y1 - delta) == b1 && bf16_bits(y1 + delta) == b1;
+    if (!safe) {
+        ff z0, z1;
+        rotate_pair_ff(x0, x1, u, sector, z0, z1);
+        b0 = rne_bf16_ff(z0);
+        b1 = rne_bf16_ff(z1);
+    }
+    return b0 | (b1 << 16);
+}
+
+template <bool kBF16, int kD>
+__global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant__ RopeArgs a)
+{
+    constexpr int kPairs = kD / 2;
+    constexpr int kEPV = kBF16 ? 8 : 4;  // elements per 16-byte vector
+    constexpr int kVPH = kD / kEPV;      // vectors per head
+    __shared__ float2 tw[kPairs];
+    __shared__ uint64_t turns[kPairs];
+    __shared__ float4 sector[5];
+
+    const int t = blockIdx.x;
+    const int pos = a.positions[t];
+    const int seq = a.seq_ids[t];
+    bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
+    int64_t blk = -1;
+    if (ok) {
+        blk = a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size];
+        ok = blk >= 0 && blk < a.num_blocks;
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
+        return;
+    }
+    const int off = pos % a.block_size;
+
+    for (int i = threadIdx.x; i < kPairs; i += blockDim.x) {
+        const uint64_t u = (uint64_t)(uint32_t)pos * a.turns[i];
+        turns[i] = u;
+        float sn, cs;
+        // fraction of a turn in [-1/2, 1/2) -> half-turns for sincospif
+        sincospif((float)(int64_t)u * 0x1p-63f, &sn, &cs);
+        tw[i] = make_float2(cs, sn);
+    }
+    if (threadIdx.x < 5) sector[threadIdx.x] = a.sector[threadIdx.x];
+    __syncthreads();
+
+    const int nq = a.hq * kVPH, nk = a.hkv * kVPH;
+    const int total = nq + 2 * nk;
+    for (int v = threadIdx.x; v < total; v += blockDim.x) {
+        int which, head, dv;
+        if (v < nq) {
+            which = 0; head = v / kVPH; dv = v - head * kVPH;
+        } else if (v < nq + nk) {
+            which = 1; head = (v - nq) / kVPH; dv = v - nq - head * kVPH;
+        } else {
+            which = 2; head = (v - nq - nk) / kVPH; dv = v - nq - nk - head * kVPH;
+        }
+        const int64_t eoff = (int64_t)dv * kEPV;
+        const char* src;
+        char* dst;
+        if (which == 0) {
+            src = (const char*)a.q + (((int64_t)t * a.hq + head) * kD + eoff) * (kBF16 ? 2 : 4);
+            dst = (char*)src;
+        } else {
+            const void* base = which == 1 ? a.k : a.v;
+            src = (const char*)base + (((int64_t)t * a.hkv + head) * kD + eoff) * (kBF16 ? 2 : 4);
+            void* pool = which == 1 ? a.k_pool : a.v_pool;
+            dst = (char*)pool + (((blk * a.hkv + head) * a.block_size + off) * kD + eoff) * (kBF16 ? 2 : 4);
+        }
+        uint4 w = *reinterpret_cast<const uint4*>(src);
+        if (which != 2) {
+            const int p0 = dv * (kEPV / 2);
+            if constexpr (kBF16) {
+                w.x = rotate_bf16_word(w.x, tw[p0 + 0], turns[p0 + 0], sector);
+                w.y = rotate_bf16_word(w.y, tw[p0 + 1], turns[p0 + 1], sector);
+                w.z = rotate_bf16_word(w.z, tw[p0 + 2], turns[p0 + 2], sector);
+                w.w = rotate_bf16_word(w.w, tw[p0 + 3], turns[p0 + 3], sector);
+            } else {
+                ff z0, z1, z2, z3;
+                rotate_pair_ff(__uint_as_float(w.x), __uint_as_float(w.y), turns[p0], sector, z0, z1);
+                rotate_pair_ff(__uint_as_float(w.z), __uint_as_float(w.w), turns[p0 + 1], sector, z2, z3);
+                w = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
+                               __float_as_uint(z3.hi));
+            }
+        }
+        *reinterpret_cast<uint4*>(dst) = w;
+    }
+}
+
+}  // namespace
+
+kvattn_status launch_rope_append(const RopeArgs& a, cudaStream_t s)
+{
+    dim3 grid(a.num_tokens), block(128);
+    const bool bf16 = a.dtype == KVATTN_BF16;
+    if (bf16 && a.d == 128) rope_append_kernel<true, 128><<<grid, block, 0, s>>>(a);
+    else if (bf16 && a.d == 64) rope_append_kernel<true, 64><<<grid, block, 0, s>>>(a);
+    else if (!bf16 && a.d == 128) rope_append_kernel<false, 128><<<grid, block, 0, s>>>(a);
+    else if (!bf16 && a.d == 64) rope_append_kernel<false, 64><<<grid, block, 0, s>>>(a);
+    else return KVATTN_ERR_UNSUPPORTED;
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace kvattn

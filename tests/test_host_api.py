@@ -1,0 +1,148 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything.
+
+Every call here fails host validation (or launches nothing), so no GPU and no
+device pointer is needed; the fake pointers are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvattn.h")
+
+
+@pytest.fixture(scope="module")
+def kv():
+    import kv_cache_attention_rope_gb300 as kv
+
+    return kv
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(kv):
+    names = header_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(kv.lib, n), f"{n} declared in kvattn.h but not exported"
+    assert sorted(kv.EXPORTED) == names
+
+
+def test_version_and_status_strings(kv):
+    assert kv.version() == 1
+    for code in range(8):
+        assert kv.status_string(code) and kv.status_string(code) != "unknown status"
+    assert kv.status_string(99) == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x7F0000001000)  # never dereferenced: every call below fails validation
+
+
+def _cache(kv, nb=8, bs=16, k=FAKE, v=FAKE):
+    return kv.CacheDesc(k, v, nb, bs)
+
+
+def _rope(kv, cfg, cache, T=1, nseq=1, maxb=1, q=FAKE):
+    return kv.lib.kvattn_rope_append(ctypes.byref(cfg) if cfg is not None else None,
+                                     ctypes.byref(cache) if cache is not None else None,
+                                     q, FAKE, FAKE, FAKE, FAKE, FAKE, nseq, maxb, T, None)
+
+
+def test_rope_append_validation(kv):
+    E = kv.STATUS_CODE
+    good = kv.make_config(8, 2, 128, kv.BF16)
+    assert _rope(kv, None, _cache(kv)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, _cache(kv), T=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, _cache(kv), nseq=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, kv.make_config(8, 2, 96, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert _rope(kv, kv.make_config(9, 3, 128, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]  # G=3
+    assert _rope(kv, kv.make_config(32, 2, 128, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]  # G=16
+    assert _rope(kv, kv.make_config(8, 3, 128, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]  # 8 % 3
+    assert _rope(kv, kv.make_config(8, 2, 128, 7), _cache(kv)) == E["KVATTN_ERR_INVALID_ARG"]  # dtype
+    assert _rope(kv, kv.make_config(8, 2, 128, kv.BF16, rope_base=-1.0), _cache(kv)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, _cache(kv, nb=0)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, _cache(kv, k=None)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, _cache(kv, k=ctypes.c_void_p(0x7F0000001004))) == E["KVATTN_ERR_INVALID_ARG"]
+    # a paged cache needs 16-token multiples for its blocks
+    assert _rope(kv, good, _cache(kv, bs=24), maxb=2) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope(kv, good, _cache(kv), maxb=0) == E["KVATTN_ERR_INVALID_ARG"]
+    # no tokens: nothing to do, nothing launched
+    assert _rope(kv, good, _cache(kv), T=0) == E["KVATTN_OK"]
+    # null q with work to do
+    assert _rope(kv, good, _cache(kv), q=None) == E["KVATTN_ERR_INVALID_ARG"]
+
+
+def _decode(kv, cfg, cache, B=2, maxlen=64, splits=0, ws=None, ws_bytes=0, out=FAKE, maxb=4):
+    return kv.lib.kvattn_decode(ctypes.byref(cfg), ctypes.byref(cache), FAKE, FAKE, maxb, FAKE, B, maxlen,
+                                splits, out, ws, ws_bytes, None)
+
+
+def test_decode_validation_and_workspace(kv):
+    E = kv.STATUS_CODE
+    cfg = kv.make_config(32, 8, 128, kv.BF16)
+    c = _cache(kv)
+    assert _decode(kv, cfg, c, B=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _decode(kv, cfg, c, splits=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _decode(kv, cfg, c, B=0) == E["KVATTN_OK"]
+    assert _decode(kv, cfg, c, out=None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _decode(kv, kv.make_config(32, 8, 80, kv.BF16), c) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert _decode(kv, cfg, c, B=10000) == E["KVATTN_ERR_UNSUPPORTED"]
+    # more than one split needs a workspace of the advertised size
+    need = kv.decode_workspace_size(cfg, 2, 4096, 4)
+    assert need >= 2 * 32 * 4 * (128 + 2) * 4
+    assert kv.decode_num_splits(cfg, 2, 4096, 4) == 4
+    assert _decode(kv, cfg, c, maxlen=4096, splits=4, ws=None) == E["KVATTN_ERR_WORKSPACE_TOO_SMALL"]
+    assert _decode(kv, cfg, c, maxlen=4096, splits=4, ws=FAKE, ws_bytes=need - 1) == \
+        E["KVATTN_ERR_WORKSPACE_TOO_SMALL"]
+    # misaligned workspace
+    assert _decode(kv, cfg, c, maxlen=4096, splits=4, ws=ctypes.c_void_p(0x7F0000001010), ws_bytes=need) == \
+        E["KVATTN_ERR_INVALID_ARG"]
+
+
+def test_decode_plan_properties(kv):
+    cfg = kv.make_config(32, 8, 128, kv.BF16)
+    # explicit split requests are honoured (at most that many chunks)
+    for maxlen in (1, 15, 16, 17, 1000, 8193):
+        for s in (1, 2, 3, 7):
+            n = kv.decode_num_splits(cfg, 4, maxlen, s)
+            assert 1 <= n <= s
+    assert kv.decode_num_splits(cfg, 4, 16, 8) == 1     # one tile cannot be split
+    assert kv.decode_workspace_size(cfg, -1, 10, 0) == 0
+    # workspace grows with the batch
+    assert kv.decode_workspace_size(cfg, 64, 4096, 4) > kv.decode_workspace_size(cfg, 8, 4096, 4)
+
+
+def test_prefill_validation(kv):
+    E = kv.STATUS_CODE
+
+    def call(cfg, cache, n=2, maxq=512, tq=1024, out=FAKE):
+        return kv.lib.kvattn_prefill_chunk(ctypes.byref(cfg), ctypes.byref(cache), FAKE, FAKE, FAKE, FAKE, 4,
+                                           n, maxq, tq, out, None)
+
+    cfg = kv.make_config(32, 8, 128, kv.BF16)
+    assert call(kv.make_config(32, 8, 128, kv.F32), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert call(kv.make_config(32, 8, 64, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert call(cfg, _cache(kv), n=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(cfg, _cache(kv), n=0) == E["KVATTN_OK"]
+    assert call(cfg, _cache(kv), out=None) == E["KVATTN_ERR_INVALID_ARG"]
+
+
+def test_get_device_status_needs_out(kv):
+    assert kv.lib.kvattn_get_device_status(None, None) == kv.STATUS_CODE["KVATTN_ERR_INVALID_ARG"]
+
+
+def test_binding_rejects_cpu_tensors(kv):
+    import torch
+
+    cfg = kv.make_config(4, 4, 64, kv.F32)
+    t = torch.zeros(4, 4, 1, 64)
+    with pytest.raises(ValueError):
+        kv.Cache(t, t)
