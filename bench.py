@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Benchmark of the kvattn hot path on GB300: one step = the host block
+allocator, RoPE + KV-cache append of the step's new tokens, chunked-prefill
+attention (mixed workload) and split-KV decode attention, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5|c4|c3|c2|c1]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Prints ONE JSON line (rank 0).  `value` is KV bytes read by the step's
+attention kernels / device step time with every input resident in HBM
+(whole job over N GPUs); `e2e` is the same metric through the C ABI from
+pinned host buffers, with the host<->device copies inside the timed region.
+For N > 1 (torchrun) each rank runs its own replica of the workload on its
+own GPU (the path shards by sequence; no collective in the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode attention KV-read GB/s and % of GB300 HBM peak; query tokens/s"
+DEFAULT_WORKLOAD = "c4"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1898.0)), float(
+            d.get("bf16_tflops_sustained", 1718.7)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+
+        try:
+            self.idx = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.idx = str(device.index)
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Step:
+    """A workload's step on one GPU, inputs resident in HBM."""
+
+    def __init__(self, wl: workloads.Workload, device):
+        import torch
+
+        import kv_cache_attention_rope_gb300 as kv
+
+        self.kv, self.torch, self.wl, self.dev = kv, torch, wl, device
+        dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.dt = dt
+        H, D, BS = wl.num_kv_heads, wl.head_dim, wl.block_size
+        per_block = 2 * BS * H * D * wl.elem_bytes
+        nb = None
+        if wl.layout == "paged":
+            nb = wl.pool_bytes // per_block if wl.pool_bytes else None
+        # batch (prefill chunks first, then decode rows); shrink a huge pool until it fits
+        while True:
+            batch = workloads.make_batch(wl, num_blocks=nb)
+            try:
+                cache = kv.Cache.empty(batch.num_blocks, H, BS, D, dt, device)
+                break
+            except torch.OutOfMemoryError:
+                nb = batch.num_blocks // 2
+                torch.cuda.empty_cache()
+        self.batch, self.cache = batch, cache
+        self.pool_bytes = batch.num_blocks * per_block
+        self.cfg = kv.make_config(wl.num_q_heads, H, D, kv.BF16 if wl.dtype == "bf16" else kv.F32)
+        nchunk = wl.chunks
+        self.nchunk = nchunk
+        past, new = batch.past, batch.new
+        # ---- host block allocator adopts the table; blocks opened by this step's
+        # tokens are handed out by the allocator every step and returned after it
+        self.alloc = kv.BlockAllocator(batch.num_blocks)
+        self.table_host = batch.block_table.copy()
+        self.open_cells = []
+        if wl.layout == "paged":
+            for r in range(batch.rows):
+                first_new_block = (int(past[r]) + BS - 1) // BS
+                last_block = (int(past[r] + new[r]) - 1) // BS
+                for c in range(first_new_block, last_block + 1):
+                    self.open_cells.append((r, c))
+            rr = np.array([r for r, _ in self.open_cells], dtype=np.int64)
+            cc = np.array([c for _, c in self.open_cells], dtype=np.int64)
+            self.open_r, self.open_c = rr, cc
+            self.table_host[rr, cc] = -1
+            self.alloc.claim(self.table_host[self.table_host >= 0])
+            ids = self.alloc.alloc(len(rr))
+            self.table_host[rr, cc] = ids
+            self.alloc.free(ids[::-1])      # LIFO: the next step gets the same ids in the same order
+            self.step_ids = ids
+        self.d_table = torch.from_numpy(self.table_host).to(device)
+        # ---- cache history (positions 0..past-1) drawn on the device
+        gen = torch.Generator(device=device)
+        gen.manual_seed(workloads.DATA_SEED)
+        rows = np.repeat(np.arange(batch.rows), past)
+        pos = np.concatenate([np.arange(p) for p in past]) if past.sum() else np.zeros(0, np.int64)
+        blk = self.table_host[rows, pos // BS].astype(np.int64)
+        off = (pos % BS).astype(np.int64)
+        step = 1 << 17
+        for s in range(0, len(pos), step):
+            b = torch.from_numpy(blk[s:s + step]).to(device)
+            o = torch.from_numpy(off[s:s + step]).to(device)
+            n = len(b)
+            cache.k_pool[b, :, o, :] = torch.randn((n, H, D), generator=gen, device=device).to(dt)
+            cache.v_pool[b, :, o, :] = torch.randn((n, H, D), generator=gen, device=device).to(dt)
+        # ---- this step's new tokens (prefill chunk tokens, then one per decode row)
+        q_l, k_l, v_l, p_l, s_l = [], [], [], [], []
+        for r in range(batch.rows):
+            q, k, v = workloads.new_tokens(wl, r, int(new[r]), int(past[r]))
+            q_l.append(q); k_l.append(k); v_l.append(v)
+            p_l.append(np.arange(past[r], past[r] + new[r], dtype=np.int32))
+            s_l.append(np.full(int(new[r]), r, dtype=np.int32))
+        self.h_q = torch.from_numpy(np.concatenate(q_l)).to(dt).pin_memory()
+        self.h_k = torch.from_numpy(np.concatenate(k_l)).to(dt).pin_memory()
+        self.h_v = torch.from_numpy(np.concatenate(v_l)).to(dt).pin_memory()
+        self.h_pos = torch.from_numpy(np.concatenate(p_l)).pin_memory()
+        self.h_sid = torch.from_numpy(np.concatenate(s_l)).pin_memory()
+        self.h_table = torch.from_numpy(self.table_host).pin_memory()
+        total = (past + new).astype(np.int32)
+        self.h_lens = torch.from_numpy(total[nchunk:].copy()).pin_memory()
+        cu = np.zeros(nchunk + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(new[:nchunk])
+        self.h_cu = torch.from_numpy(cu).pin_memory()
+        self.h_prefix = torch.from_numpy(past[:nchunk].astype(np.int32)).pin_memory()
+        self.q = self.h_q.to(device)
+        self.k = self.h_k.to(device)
+        self.v = self.h_v.to(device)
+        self.pos = self.h_pos.to(device)
+        self.sid = self.h_sid.to(device)
+        self.lens = self.h_lens.to(device)
+        self.cu = self.h_cu.to(device)
+        self.prefix = self.h_prefix.to(device)
+        self.n_dec = batch.rows - nchunk
+        self.n_tok = int(new.sum())
+        self.chunk_tokens = int(new[:nchunk].sum())
+        self.max_len = int(total[nchunk:].max()) if self.n_dec else 1
+        self.max_q = int(new[:nchunk].max()) if nchunk else 0
+        self.q_dec = self.q[self.chunk_tokens:]
+        self.q_pre = self.q[:self.chunk_tokens]
+        self.out_dec = torch.empty_like(self.q_dec)
+        self.out_pre = torch.empty_like(self.q_pre)
+        self.d_table_dec = self.d_table[nchunk:]
+        self.d_table_pre = self.d_table[:nchunk]
+        self.splits = kv.decode_num_splits(self.cfg, self.n_dec, self.max_len, 0) if self.n_dec else 0
+        nws = kv.decode_workspace_size(self.cfg, max(1, self.n_dec), self.max_len, 0)
+        self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=device)
+        self.h_out = torch.empty(self.out_dec.shape, dtype=dt).pin_memory()
+        # algorithmic bytes / flops
+        E = wl.elem_bytes
+        self.kv_bytes_decode = workloads.kv_bytes_read(wl, total[nchunk:])
+        self.kv_bytes_prefill = workloads.kv_bytes_read(wl, total[:nchunk])
+        self.rope_bytes = self.n_tok * 2 * (wl.num_q_heads + 2 * H) * D * E
+        pre_flops = 0
+        for c in range(nchunk):
+            P, n = int(past[c]), int(new[c])
+            pre_flops += 4 * D * wl.num_q_heads * int(np.sum(P + np.arange(n) + 1))
+        self.prefill_flops = pre_flops
+        self.launches_per_step = 1 + (1 if self.n_dec else 0) + (1 if self.splits > 1 else 0) + (1 if nchunk else 0)
+
+    # host block allocator: hand out the blocks this step's tokens open, return them after
+    def alloc_begin(self):
+        if self.open_cells:
+            ids = self.alloc.alloc(len(self.open_r))
+            self.table_host[self.open_r, self.open_c] = ids
+            return ids
+        return None
+
+    def alloc_end(self, ids):
+        if ids is not None:
+            self.alloc.free(ids[::-1])
+
+    def launch(self, ev=None):
+        kv = self.kv
+        ids = self.alloc_begin()
+        if ev is not None:
+            ev[0].record()
+        kv.rope_append(self.cfg, self.cache, self.q, self.k, self.v, self.pos, self.sid, self.d_table)
+        if ev is not None:
+            ev[1].record()
+        if self.nchunk:
+            kv.prefill_chunk(self.cfg, self.cache, self.q_pre, self.cu, self.prefix, self.d_table_pre, self.max_q,
+                             out=self.out_pre)
+        if ev is not None:
+            ev[2].record()
+        if self.n_dec:
+            kv.decode(self.cfg, self.cache, self.q_dec, self.d_table_dec, self.lens, self.max_len, out=self.out_dec,
+                      workspace=self.ws)
+        if ev is not None:
+            ev[3].record()
+        self.alloc_end(ids)
+
+    def launch_e2e(self):
+        """Same step from pinned host buffers: inputs up, kernels, output down."""
+        ids = self.alloc_begin()
+        self.h_table.copy_(self.torch.from_numpy(self.table_host))
+        for d, h in ((self.q, self.h_q), (self.k, self.h_k), (self.v, self.h_v), (self.pos, self.h_pos),
+                     (self.sid, self.h_sid), (self.d_table, self.h_table), (self.lens, self.h_lens),
+                     (self.cu, self.h_cu), (self.prefix, self.h_prefix)):
+            d.copy_(h, non_blocking=True)
+        kv = self.kv
+        kv.rope_append(self.cfg, self.cache, self.q, self.k, self.v, self.pos, self.sid, self.d_table)
+        if self.nchunk:
+            kv.prefill_chunk(self.cfg, self.cache, self.q_pre, self.cu, self.prefix, self.d_table_pre, self.max_q,
+                             out=self.out_pre)
+        if self.n_dec:
+            kv.decode(self.cfg, self.cache, self.q_dec, self.d_table_dec, self.lens, self.max_len, out=self.out_dec,
+                      workspace=self.ws)
+            self.h_out.copy_(self.out_dec, non_blocking=True)
+        self.alloc_end(ids)
+
+    def h2d_bytes(self) -> int:
+        ts = (self.h_q, self.h_k, self.h_v, self.h_pos, self.h_sid, self.h_table, self.h_lens, self.h_cu,
+              self.h_prefix)
+        return int(sum(t.numel() * t.element_size() for t in ts))
+
+    def d2h_bytes(self) -> int:
+        return int(self.h_out.numel() * self.h_out.element_size()) if self.n_dec else 0
+
+
+def oracle_sample(wl: workloads.Workload, target_s: float = 12.0, max_rows: int = 8):
+    """Times the oracle (as it stands) on a bounded sample of the workload's decode rows:
+    RoPE + rounding + append of each row's new token, then attention of its query.
+    Returns (GB/s of KV bytes, cores, sample description, per-pass seconds)."""
+    import oracle
+
+    batch = workloads.make_batch(wl, num_blocks=1 << 22)
+    dec = list(range(wl.chunks, batch.rows))
+    rows = dec[:max_rows]
+    BS, H, D = wl.block_size, wl.num_kv_heads, wl.head_dim
+    need = [(int(batch.total[r]) + BS - 1) // BS for r in rows]
+    table = np.full((len(rows), max(need)), -1, dtype=np.int32)
+    o = 0
+    for i, n in enumerate(need):
+        table[i, :n] = np.arange(o, o + n, dtype=np.int32)
+        o += n
+    cache = oracle.Cache(o, BS, H, D)
+    od = oracle.BF16 if wl.dtype == "bf16" else oracle.F32
+    for i, r in enumerate(rows):
+        p = int(batch.past[r])
+        k, v = workloads.history(wl, r, p)
+        oracle.append(cache, oracle.round_to(k, od), oracle.round_to(v, od), np.arange(p), np.full(p, i, np.int32),
+                      table)
+    news = [workloads.new_tokens(wl, r, 1, int(batch.past[r])) for r in rows]
+    kvb = workloads.kv_bytes_read(wl, batch.total[rows])
+
+    def one_pass():
+        qs = []
+        for i, r in enumerate(rows):
+            p = int(batch.past[r])
+            q, k, v = news[i]
+            kh = oracle.round_to(oracle.rope(k.astype(np.float64), [p]), od)
+            oracle.append(cache, kh, oracle.round_to(v, od), [p], [i], table)
+            qs.append(oracle.round_to(oracle.rope(q.astype(np.float64), [p]), od)[0])
+        oracle.attend(cache, np.stack(qs), list(range(len(rows))), [int(batch.past[r]) for r in rows], table,
+                      wl.num_q_heads)
+
+    t0 = time.perf_counter()
+    one_pass()
+    t1 = time.perf_counter()
+    return kvb, oracle.num_cores(), f"{len(rows)} decode rows of {wl.key} (their lengths, all heads)", t1 - t0, one_pass
+
+
+def cpu_baseline(wl, target_s: float = 12.0):
+    kvb, cores, desc, t_one, one_pass = oracle_sample(wl)
+    reps = max(1, min(200, int(target_s / max(t_one, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        one_pass()
+    dt = time.perf_counter() - t0
+    return {"value": kvb * reps / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{desc}, {reps} passes in {dt:.1f} s (fp64 C, {cores} threads)"}
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = workloads.WORKLOADS[args.workload]
+    st = Step(wl, dev)
+    hbm, bf16_burst, bf16_sus, peak_src = peaks()
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        st.launch()
+    torch.cuda.synchronize()
+    status = st.kv.get_device_status()
+    if status:
+        raise RuntimeError(f"device status {st.kv.STATUS.get(status)} after warm-up")
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(stream)
+    for i in range(K):
+        st.launch(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed = start.elapsed_time(end) / 1e3
+    t_rope = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_pre = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    t_dec = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    status = st.kv.get_device_status()
+    if status:
+        raise RuntimeError(f"device status {st.kv.STATUS.get(status)} in the timed region")
+    # e2e through host buffers
+    e2e = None
+    e2e_t = 0.0
+    if not args.no_e2e:
+        for _ in range(3):
+            st.launch_e2e()
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(K):
+            st.launch_e2e()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_t = s2.elapsed_time(e2) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed, e2e_t], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed, e2e_t = float(t[0]), float(t[1])
+    step_bytes = st.kv_bytes_decode + st.kv_bytes_prefill
+    value = world * K * step_bytes / elapsed / 1e9
+    if not args.no_e2e:
+        e2e = {"value": world * K * step_bytes / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": st.h2d_bytes(),
+               "d2h_bytes_per_step": st.d2h_bytes(), "ms_per_step": 1e3 * e2e_t / K}
+    # dominant kernel roofline
+    parts = {"decode": t_dec, "prefill": t_pre, "rope_append": t_rope}
+    dom = max(parts, key=parts.get)
+    if dom == "prefill":
+        ach = st.prefill_flops / t_pre / 1e12
+        roof = {"kernel": "prefill_chunk", "bound": "tensor", "achieved": ach, "peak": bf16_sus, "unit": "TFLOP/s",
+                "frac": ach / bf16_sus, "traffic": None, "peak_source": f"bf16_tflops_sustained ({peak_src})"}
+    else:
+        k = "decode" if dom == "decode" else "rope_append"
+        by = st.kv_bytes_decode if k == "decode" else st.rope_bytes
+        ach = by / parts[dom] / 1e9
+        roof = {"kernel": "decode_split+decode_combine" if k == "decode" else "rope_append", "bound": "hbm",
+                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                "peak_source": f"hbm_gbs ({peak_src})"}
+    out = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": f"{wl.key}: {wl.name}", "decode_seqs": st.n_dec, "prefill_chunks": st.nchunk,
+                   "query_tokens": st.n_tok, "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+                   "head_dim": wl.head_dim, "block_size": wl.block_size, "pool_bytes": st.pool_bytes,
+                   "kv_bytes_per_step": step_bytes, "decode_splits": st.splits,
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of KV per step)"
+                   if step_bytes > 2e8 else "L2-resident: KV smaller than L2, not flushed",
+                   "parallelism": f"replicas x{world}"},
+        "query_tokens_per_s": world * K * st.n_tok / elapsed,
+        "hbm_frac": (st.kv_bytes_decode / t_dec / 1e9) / hbm if st.n_dec else None,
+        "kernels_ms": {k: 1e3 * v for k, v in parts.items()},
+        "decode_kv_gbs": st.kv_bytes_decode / t_dec / 1e9 if st.n_dec else None,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": K * st.launches_per_step,
+        "clocks": ck,
+    }
+    if st.nchunk:
+        out["prefill_tflops"] = st.prefill_flops / t_pre / 1e12
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    return out
+
+
+def run_reference(args, world):
+    """The fp64 oracle as it stands, on this host's cores, same metric and workload."""
+    wl = workloads.WORKLOADS[args.workload]
+    kvb, cores, desc, _, one_pass = oracle_sample(wl)
+    for _ in range(args.warmup):
+        one_pass()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_pass()
+    dt = time.perf_counter() - t0
+    v = kvb * args.steps / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.key}: {wl.name}", "sample": desc},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group(backend="nccl")
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

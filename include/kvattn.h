@@ -224,6 +224,11 @@ kvattn_status kvattn_alloc_blocks(kvattn_allocator* a, int32_t n, int32_t* out_i
  * as many times as it has references). */
 kvattn_status kvattn_free_blocks(kvattn_allocator* a, const int32_t* ids, int32_t n);
 
+/* Takes the given free ids (refcount 1), for adopting an existing block
+ * table: INVALID_ARG and nothing changes if one is out of range, not free,
+ * or repeated. */
+kvattn_status kvattn_claim_blocks(kvattn_allocator* a, const int32_t* ids, int32_t n);
+
 /* Adds one reference to each (allocated) id: INVALID_ARG and nothing changes
  * if one is not allocated. */
 kvattn_status kvattn_share_blocks(kvattn_allocator* a, const int32_t* ids, int32_t n);

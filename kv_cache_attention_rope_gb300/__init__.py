@@ -35,7 +35,7 @@ EXPORTED = [
     "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_decode_workspace_size",
     "kvattn_decode_num_splits", "kvattn_decode", "kvattn_prefill_chunk", "kvattn_get_device_status",
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
-    "kvattn_share_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
+    "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
     "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
 ]
 
@@ -79,6 +79,7 @@ def _load():
         "kvattn_alloc_blocks": ([p, i32, p], ctypes.c_int),
         "kvattn_free_blocks": ([p, p, i32], ctypes.c_int),
         "kvattn_share_blocks": ([p, p, i32], ctypes.c_int),
+        "kvattn_claim_blocks": ([p, p, i32], ctypes.c_int),
         "kvattn_allocator_num_free": ([p], i64),
         "kvattn_allocator_num_failures": ([p], i64),
         "kvattn_allocator_refcount": ([p, i32], i32),
@@ -276,6 +277,13 @@ class BlockAllocator:
 
         a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
         check(lib.kvattn_share_blocks(self._h, a.ctypes.data_as(ctypes.c_void_p), a.size), "kvattn_share_blocks")
+
+    def claim(self, ids) -> None:
+        """Takes specific free ids (adopting an existing block table)."""
+        import numpy as np
+
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        check(lib.kvattn_claim_blocks(self._h, a.ctypes.data_as(ctypes.c_void_p), a.size), "kvattn_claim_blocks")
 
     def grow(self, table_row, block_size: int, cur_len: int, new_len: int) -> None:
         """Allocates blocks so the int32 numpy row covers new_len tokens (in place)."""

@@ -35,7 +35,13 @@ def _stale(obj: str, deps: list[str]) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    import platform
+
     os.makedirs(BUILD, exist_ok=True)
+    stamp = os.path.join(BUILD, "host_arch")
+    arch = platform.machine()
+    if not os.path.exists(stamp) or open(stamp).read() != arch or not os.path.exists(LIB):
+        force = True      # objects from another host architecture or a missing library
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "kvattn.h"))
     jobs = []
@@ -66,6 +72,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
         os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(arch)
     return LIB
 
 

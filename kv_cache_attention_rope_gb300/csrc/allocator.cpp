@@ -21,6 +21,15 @@ struct kvattn_allocator {
     int64_t failures = 0;
 };
 
+// Removes the ids whose refcount was just set from the free stack (one pass).
+static void compact_free_stack(kvattn_allocator* a)
+{
+    size_t w = 0;
+    for (size_t r = 0; r < a->free_ids.size(); ++r)
+        if (a->refs[(size_t)a->free_ids[r]] == 0) a->free_ids[w++] = a->free_ids[r];
+    a->free_ids.resize(w);
+}
+
 extern "C" {
 
 kvattn_status kvattn_allocator_create(int64_t num_blocks, kvattn_allocator** out)
@@ -89,6 +98,22 @@ kvattn_status kvattn_free_blocks(kvattn_allocator* a, const int32_t* ids, int32_
         int32_t& r = a->refs[(size_t)ids[i]];
         if (--r == 0) a->free_ids.push_back(ids[i]);
     }
+    return KVATTN_OK;
+}
+
+kvattn_status kvattn_claim_blocks(kvattn_allocator* a, const int32_t* ids, int32_t n)
+{
+    if (!a || n < 0 || (n > 0 && !ids)) return KVATTN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(a->mu);
+    std::vector<int32_t> sorted(ids, ids + n);
+    std::sort(sorted.begin(), sorted.end());
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t id = sorted[(size_t)i];
+        if (id < 0 || (size_t)id >= a->refs.size() || a->refs[(size_t)id] != 0) return KVATTN_ERR_INVALID_ARG;
+        if (i > 0 && sorted[(size_t)i - 1] == id) return KVATTN_ERR_INVALID_ARG;
+    }
+    for (int32_t i = 0; i < n; ++i) a->refs[(size_t)ids[i]] = 1;
+    if (n > 0) compact_free_stack(a);
     return KVATTN_OK;
 }
 

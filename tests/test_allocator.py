@@ -143,3 +143,20 @@ def test_table_grow_is_all_or_nothing():
     with pytest.raises(kv.KvattnError):
         a.grow(row, 16, 0, 64)     # needs 4 blocks, 3 exist
     assert (row == -1).all() and a.num_free == 3 and a.num_failures == 1
+
+
+def test_claim_adopts_an_existing_table():
+    a = kv.BlockAllocator(10)
+    a.claim([7, 2, 5])
+    assert a.num_free == 7 and a.refcount(7) == 1
+    with pytest.raises(kv.KvattnError):
+        a.claim([1, 2])          # 2 is taken: nothing changes
+    assert a.refcount(1) == 0
+    with pytest.raises(kv.KvattnError):
+        a.claim([3, 3])          # repeated
+    with pytest.raises(kv.KvattnError):
+        a.claim([10])            # out of range
+    got = set(a.alloc(7).tolist())
+    assert got == {0, 1, 3, 4, 6, 8, 9}
+    a.free([2])
+    assert a.alloc(1).tolist() == [2]

@@ -94,6 +94,7 @@ def test_rope_append_reports_bad_index_and_writes_the_rest(kvattn_lib):
     cfg = kv.make_config(4, 4, 64, kv.BF16)
     cache = kv.Cache.empty(4, 4, 16, 64, torch.bfloat16, dev)
     cache.k_pool.zero_()
+    cache.v_pool.zero_()
     table = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device=dev)   # block 9 does not exist
     T = 4
     q = torch.randn(T, 4, 64, device=dev).to(torch.bfloat16)
