@@ -168,6 +168,34 @@ kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache,
                             void* stream);
 
 /*
+ * kvattn_decode_static_scratch -- kvattn_decode without a caller workspace,
+ * for callers that cannot allocate device memory when they run a decode step
+ * (for example an engine that has already given nearly all HBM to its own
+ * KV-cache pool and arenas, or code inside a host framework's operator
+ * interface that has no device allocator and must not call cudaMalloc or
+ * cudaFree, which would synchronise the device mid-step).  No counterpart on
+ * the pages: it is a deployment convenience of this library.
+ *
+ * Same arguments, results and errors as kvattn_decode, minus the workspace.
+ * The partial results live in a fixed 32 MiB array in the library's own
+ * device memory (every GPU that loads the library holds it until the process
+ * exits); a call whose kvattn_decode_workspace_size(cfg, batch, max_seq_len,
+ * num_splits) exceeds 32 MiB returns KVATTN_ERR_WORKSPACE_TOO_SMALL and
+ * launches nothing.  The function allocates nothing (no cudaMalloc, cudaFree
+ * or allocating library call).  Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls on a device
+ * share the one array, so calls whose work overlaps on the GPU (different
+ * streams, or concurrent host threads) race and must be serialised by the
+ * caller.
+ */
+kvattn_status kvattn_decode_static_scratch(const kvattn_config* cfg, const kvattn_cache* cache,
+                                           const void* q, const int32_t* block_table,
+                                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                           int32_t batch, int32_t max_seq_len, int32_t num_splits,
+                                           void* out, void* stream);
+
+/*
  * kvattn_prefill_chunk -- causal attention of chunks of new query tokens
  * against their sequences' caches, which already hold the chunks' own keys
  * (call kvattn_rope_append for the chunk tokens first).

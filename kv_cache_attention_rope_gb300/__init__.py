@@ -33,7 +33,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTED = [
     "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_decode_workspace_size",
-    "kvattn_decode_num_splits", "kvattn_decode", "kvattn_prefill_chunk", "kvattn_get_device_status",
+    "kvattn_decode_num_splits", "kvattn_decode", "kvattn_decode_static_scratch", "kvattn_prefill_chunk", "kvattn_get_device_status",
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
     "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
     "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
@@ -72,6 +72,7 @@ def _load():
         "kvattn_decode_workspace_size": ([cfgp, i32, i32, i32], sz),
         "kvattn_decode_num_splits": ([cfgp, i32, i32, i32], i32),
         "kvattn_decode": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p, sz, p], ctypes.c_int),
+        "kvattn_decode_static_scratch": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p], ctypes.c_int),
         "kvattn_prefill_chunk": ([cfgp, cachep, p, p, p, p, i32, i32, i32, i32, p, p], ctypes.c_int),
         "kvattn_get_device_status": ([p, ctypes.POINTER(i32)], ctypes.c_int),
         "kvattn_allocator_create": ([i64, ctypes.POINTER(p)], ctypes.c_int),
