@@ -43,6 +43,10 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--rows", type=int, default=0,
+                   help="use only the first N decode rows of the workload (profiling small cases)")
+    p.add_argument("--compact-pool", action="store_true",
+                   help="pool of twice the blocks the batch needs instead of the workload's pool size")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -117,7 +121,7 @@ class ClockSampler:
 class Step:
     """A workload's step on one GPU, inputs resident in HBM."""
 
-    def __init__(self, wl: workloads.Workload, device):
+    def __init__(self, wl: workloads.Workload, device, rows: int = 0, compact_pool: bool = False):
         import torch
 
         import kv_cache_attention_rope_gb300 as kv
@@ -128,11 +132,18 @@ class Step:
         H, D, BS = wl.num_kv_heads, wl.head_dim, wl.block_size
         per_block = 2 * BS * H * D * wl.elem_bytes
         nb = None
+        subset = None
+        if rows:
+            subset = list(range(wl.chunks)) + list(range(wl.chunks, min(wl.chunks + rows, wl.chunks + wl.decode_batch)))
         if wl.layout == "paged":
-            nb = wl.pool_bytes // per_block if wl.pool_bytes else None
+            if compact_pool:
+                probe = workloads.make_batch(wl, num_blocks=1 << 30, rows_subset=subset)
+                nb = int(2 * ((probe.total + BS - 1) // BS).sum())
+            elif wl.pool_bytes:
+                nb = wl.pool_bytes // per_block
         # batch (prefill chunks first, then decode rows); shrink a huge pool until it fits
         while True:
-            batch = workloads.make_batch(wl, num_blocks=nb)
+            batch = workloads.make_batch(wl, num_blocks=nb, rows_subset=subset)
             try:
                 cache = kv.Cache.empty(batch.num_blocks, H, BS, D, dt, device)
                 break
@@ -354,7 +365,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     wl = workloads.WORKLOADS[args.workload]
-    st = Step(wl, dev)
+    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool)
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
@@ -427,7 +438,8 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": f"{wl.key}: {wl.name}", "decode_seqs": st.n_dec, "prefill_chunks": st.nchunk,
+        "config": {"workload": f"{wl.key}: {wl.name}" + (f" (first {args.rows} decode rows)" if args.rows else ""),
+                   "decode_seqs": st.n_dec, "prefill_chunks": st.nchunk,
                    "query_tokens": st.n_tok, "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
                    "head_dim": wl.head_dim, "block_size": wl.block_size, "pool_bytes": st.pool_bytes,
                    "kv_bytes_per_step": step_bytes, "decode_splits": st.splits,

@@ -1,5 +1,6 @@
 // C ABI of kvattn: argument validation, per-device set-up, dispatch to the
 // kernels.  Every check the host can make is made here, before any launch.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -185,20 +186,35 @@ int32_t kvattn_decode_num_splits(const kvattn_config* cfg, int32_t batch, int32_
 {
     if (!config_ok(cfg) || config_supported(cfg) != KVATTN_OK || batch < 0 || max_seq_len < 0 || num_splits < 0)
         return 0;
-    const DecodePlan p = decode_plan(batch, cfg->num_kv_heads, cfg->num_q_heads / cfg->num_kv_heads,
-                                     max_seq_len, num_splits);
-    return p.max_chunks;
+    return decode_plan(batch, cfg->num_kv_heads, cfg->num_q_heads / cfg->num_kv_heads, max_seq_len, num_splits)
+        .slots;
 }
+
+namespace {
+// Workspace: [batch][segments] int32 piece counts | [batch][hq][slots][D] f32
+// partial outputs | [batch][hq][slots][2] f32 (max, sum); each 256-byte aligned.
+struct WorkspaceLayout {
+    size_t nslots_off, o_off, ml_off, bytes;
+};
+WorkspaceLayout workspace_layout(const kvattn_config* cfg, int32_t batch, int32_t slots)
+{
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    WorkspaceLayout w;
+    const size_t rows = (size_t)batch * cfg->num_q_heads * slots;
+    w.nslots_off = 0;
+    w.o_off = up((size_t)batch * decode_segments(cfg->num_q_heads, cfg->num_kv_heads) * 4);
+    w.ml_off = w.o_off + up(rows * cfg->head_dim * 4);
+    w.bytes = std::max<size_t>(256, w.ml_off + up(rows * 2 * 4));
+    return w;
+}
+}  // namespace
 
 size_t kvattn_decode_workspace_size(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len,
                                     int32_t num_splits)
 {
-    const int32_t chunks = kvattn_decode_num_splits(cfg, batch, max_seq_len, num_splits);
-    if (chunks <= 0) return 0;
-    const size_t rows = (size_t)batch * cfg->num_q_heads * chunks;
-    const size_t o_bytes = (rows * cfg->head_dim * 4 + 255) / 256 * 256;
-    const size_t ml_bytes = (rows * 2 * 4 + 255) / 256 * 256;
-    return std::max<size_t>(256, o_bytes + ml_bytes);
+    const int32_t slots = kvattn_decode_num_splits(cfg, batch, max_seq_len, num_splits);
+    if (slots <= 0) return 0;
+    return workspace_layout(cfg, batch, slots).bytes;
 }
 
 kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,
@@ -214,12 +230,11 @@ kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache,
     if (batch > 8192) return KVATTN_ERR_UNSUPPORTED;
     if (!q || !block_table || !seq_lens || !out) return KVATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return KVATTN_ERR_INVALID_ARG;
-    const size_t need = kvattn_decode_workspace_size(cfg, batch, max_seq_len, num_splits);
-    if (need == 0) return KVATTN_ERR_INVALID_ARG;
     const DecodePlan p = decode_plan(batch, cfg->num_kv_heads, cfg->num_q_heads / cfg->num_kv_heads, max_seq_len,
                                      num_splits);
-    if (p.max_chunks > 1) {
-        if (!workspace || workspace_bytes < need) return KVATTN_ERR_WORKSPACE_TOO_SMALL;
+    const WorkspaceLayout wl = workspace_layout(cfg, batch, p.slots);
+    if (p.slots > 1) {
+        if (!workspace || workspace_bytes < wl.bytes) return KVATTN_ERR_WORKSPACE_TOO_SMALL;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return KVATTN_ERR_INVALID_ARG;
     }
     DecodeArgs a;
@@ -230,18 +245,18 @@ kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache,
     a.block_table = block_table;
     a.seq_lens = seq_lens;
     a.out = out;
-    const size_t rows = (size_t)batch * cfg->num_q_heads * p.max_chunks;
-    a.part_o = static_cast<float*>(workspace);
-    a.part_ml = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                     (rows * cfg->head_dim * 4 + 255) / 256 * 256)
-                          : nullptr;
+    if (p.slots > 1) {
+        char* w = static_cast<char*>(workspace);
+        a.nslots = reinterpret_cast<int32_t*>(w + wl.nslots_off);
+        a.part_o = reinterpret_cast<float*>(w + wl.o_off);
+        a.part_ml = reinterpret_cast<float*>(w + wl.ml_off);
+    }
     a.num_blocks = cache->num_blocks;
     a.block_size = cache->block_size;
     a.max_blocks = max_blocks_per_seq;
     a.batch = batch;
     a.max_seq_len = max_seq_len;
-    a.splits = p.max_chunks;
-    a.chunk_tiles = p.chunk_tiles;
+    a.splits = p.slots;
     a.hq = cfg->num_q_heads;
     a.hkv = cfg->num_kv_heads;
     a.d = cfg->head_dim;

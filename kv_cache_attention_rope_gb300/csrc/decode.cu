@@ -4,26 +4,31 @@
 //   out[b][j] = softmax_i(q[b][j] . K_b[i] * scale) V_b[i],  i < seq_lens[b]
 // ("From-scratch AI inference engine" page, section 3.3: with a cache the
 // new token's query has length 1 and sees all S cached keys; section 3.1:
-// scale 1/sqrt(d_k) before the softmax).  The keys of a sequence are cut into
-// chunks; each chunk yields a partial (running max m, running sum l, l-
-// normalised weighted V) with the online softmax of section 3.4 of the same
-// page, and decode_combine merges the chunks of a sequence.
+// scale 1/sqrt(d_k) before the softmax).  The keys of a sequence may be cut
+// into pieces; each piece yields a partial (running max m, running sum l,
+// l-normalised weighted V) with the online softmax of section 3.4 of the same
+// page, and decode_combine merges the pieces of a sequence.
 //
 // How (GB300 design):
-//  - Persistent grid: every CTA holds a prefix sum of the chunk counts of the
-//    batch and walks work items (sequence, chunk, KV head) round-robin, so
-//    chunks of equal size spread evenly over the SMs with no empty CTAs.
-//  - Warp specialisation: one producer warp streams 16-token tiles of K and V
-//    for one KV head (16 x D contiguous elements of one cache block) with
-//    1-D TMA bulk copies into an mbarrier-tracked ring of stages; the block
-//    ids for 32 upcoming tiles are fetched with one coalesced load.  The ring
-//    keeps tens of KB in flight per CTA, which is what HBM needs.
-//  - Consumer warps each take whole tiles round-robin and keep their own
+//  - Flat work decomposition: the 16-token tiles of all (sequence, KV head)
+//    segments form one stream; every persistent CTA takes an equal
+//    contiguous range of it (segments are cut where ranges meet), so the
+//    load is balanced to one tile whatever the length mix.  Each CTA derives
+//    the ranges from a prefix sum of the batch's tile counts held in shared
+//    memory.  A cap on the pieces per segment bounds the workspace.
+//  - Warp specialisation: one producer warp streams tiles of K and V (16 x D
+//    contiguous elements of one block and KV head) with 1-D TMA bulk copies
+//    into an mbarrier-tracked ring of stages; the block ids of the next 32
+//    tiles come from one coalesced load.  The ring keeps tens of KB in flight
+//    per CTA, which is what HBM needs.
+//  - Consumer warps take whole tiles round-robin and keep their own
 //    online-softmax state.  All query heads of a GQA group are computed from
-//    the one copy of the tile in shared memory (the KV bytes are read once).
-//    A warp splits into token groups; a lane owns a slice of D, computes
-//    partial dot products with packed f32x2 FMAs, and a butterfly
-//    reduce-scatter over the group's lanes finishes the scores.
+//    the one copy of a tile in shared memory (KV bytes are read once).  A warp
+//    splits into token groups; a lane owns a slice of D, forms partial dot
+//    products with packed f32x2 FMAs, and a select-free butterfly
+//    reduce-scatter over the group's lanes finishes the scores (each lane
+//    holds its partials in a lane-dependent XOR order so that every level
+//    keeps the lower half and receives the upper half).
 //  - All waits are bounded (1 s); on a timeout the CTA records
 //    KVATTN_ERR_TIMEOUT and drains without further waiting.
 #include <algorithm>
@@ -38,7 +43,8 @@ namespace {
 constexpr int kTile = 16;  // tokens per tile
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxBatch = 8192;  // prefix array lives in shared memory
+constexpr int kMinPer = 4;  // fewest tiles in a CTA's range (flat mode)
+constexpr int kCtasPerSm = 3;  // residency the register and shared-memory budgets aim at
 
 // --------------------------------------------------------- packed f32x2 math
 
@@ -61,6 +67,12 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 
 // 16 bytes of cache elements -> f32x2 pairs (element 2i in the low half)
 template <bool kBF16>
@@ -77,27 +89,23 @@ __device__ __forceinline__ void unpack16(const uint4& w, uint64_t* out)
     }
 }
 
-// Butterfly reduce-scatter of N values over the lanes xor-reachable with
-// offsets O, O/2, ..., 1: afterwards value i of this lane holds the full sum
-// of index (sum over steps of bit*half) + i.
+// Select-free butterfly reduce-scatter of N values over lanes xor-reachable
+// with offsets O, O/2, ..., 1.  Every level keeps the lower half and adds the
+// partner's upper half; that is a reduce-scatter because each lane stores its
+// values XOR-permuted by a lane-dependent mask (see Traits::mask).
 template <int N, int O>
 struct Bfly {
-    static __device__ __forceinline__ void run(float* v, int lane)
+    static __device__ __forceinline__ void run(float* v)
     {
         if constexpr (O >= 1) {
             if constexpr (N > 1) {
                 constexpr int H = N / 2;
-                const bool up = (lane & O) != 0;
 #pragma unroll
-                for (int i = 0; i < H; ++i) {
-                    const float send = up ? v[i] : v[i + H];
-                    const float keep = up ? v[i + H] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-                }
-                Bfly<H, O / 2>::run(v, lane);
+                for (int i = 0; i < H; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + H], O);
+                Bfly<H, O / 2>::run(v);
             } else {
                 v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-                Bfly<1, O / 2>::run(v, lane);
+                Bfly<1, O / 2>::run(v);
             }
         }
     }
@@ -120,12 +128,14 @@ struct Traits {
     static constexpr int kTileBytes = kTile * kD * kE;      // K (or V) bytes of a full tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static_assert(kNC >= 1 && kDPL % kCE == 0, "lane slice must hold whole 16-byte chunks");
-    static_assert(kBW >= 1, "head block");
+    static_assert(kBW >= 1 && kTPG % 2 == 0, "tile split");
+    // logical score index held first by this lane after the reduction; it is
+    // also the XOR mask of the lane's partial-score layout
+    static __device__ __forceinline__ int mask(int sub) { return kV >= kLPG ? sub * kR : sub / kDup; }
 };
 
 struct SharedLayout {
-    int stages;
-    int ring_off, merge_off, pbuf_off, prefix_off, bar_off, flag_off, bytes;
+    int ring_off, merge_off, pbuf_off, prefix_off, bar_off, flag_off, bytes;  // pbuf aliases merge
 };
 
 template <bool kBF16, int kD, int kGT>
@@ -133,14 +143,15 @@ __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
 {
     using T = Traits<kBF16, kD, kGT>;
     SharedLayout L;
-    L.stages = stages;
     int off = 0;
     L.ring_off = off;
     off += stages * T::kStageBytes;
+    // per consumer warp: its merge slot (kGT x (D + 2) floats, written at the
+    // end of a piece) doubles as its probability buffer while tiles stream
+    static_assert(T::kTG * T::kV * 8 <= kGT * (kD + 2) * 4, "probability buffer fits the merge slot");
     L.merge_off = off;
     off += kConsumerWarps * kGT * (kD + 2) * 4;
-    L.pbuf_off = off;
-    off += kConsumerWarps * T::kTG * T::kV * 4;
+    L.pbuf_off = L.merge_off;
     L.prefix_off = off;
     off += ((batch + 1) * 4 + 15) / 16 * 16;
     L.bar_off = off;
@@ -151,64 +162,91 @@ __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
     return L;
 }
 
-struct ItemInfo {
-    int b, chunk, h, hsub, nchunks, len;
+// One contiguous run of tiles of one (sequence, KV head [, q-head subgroup])
+// segment, and where its result goes.
+struct Piece {
+    int b, hh, t0, t1, len;
+    int slot, nslots;  // partial slot of this piece among the segment's pieces
 };
 
-// Work item `idx` -> (sequence, chunk, kv head, q-head subgroup) and its tiles.
-__device__ __forceinline__ ItemInfo decode_item(int idx, const int* prefix, int batch, int heads_x_sub,
-                                                int nsub, const DecodeArgs& a)
-{
-    ItemInfo it;
-    const int hh = idx % heads_x_sub;
-    const int rest = idx / heads_x_sub;
-    // first b with prefix[b+1] > rest
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid + 1] > rest) hi = mid; else lo = mid + 1;
+// Walks the pieces of this CTA.  Producer and consumers run identical copies.
+struct PieceIter {
+    const int* P;  // P[b]: first stream tile of sequence b (P[batch] = total)
+    int batch, hh_count, per, r, r1, b, seg;
+    bool flat;
+
+    __device__ bool next(Piece& pc, const DecodeArgs& a)
+    {
+        if (flat) {
+            if (r >= r1) return false;
+            while (P[b + 1] <= r) ++b;
+            const int nt = (P[b + 1] - P[b]) / hh_count;
+            const int off = r - P[b];
+            const int hh = off / nt;
+            const int t0 = off - hh * nt;
+            const int take = min(nt - t0, r1 - r);
+            const int s0 = P[b] + hh * nt;
+            const int first = s0 / per, last = (s0 + nt - 1) / per;
+            pc.b = b;
+            pc.hh = hh;
+            pc.t0 = t0;
+            pc.t1 = t0 + take;
+            pc.slot = (int)blockIdx.x - first;
+            pc.nslots = last - first + 1;
+            r += take;
+        } else {
+            while (true) {
+                if (seg >= batch * hh_count) return false;
+                const int bb = seg / hh_count, hh = seg - bb * hh_count;
+                const int nt = (P[bb + 1] - P[bb]) / hh_count;
+                seg += gridDim.x;
+                if (nt == 0) continue;
+                pc.b = bb;
+                pc.hh = hh;
+                pc.t0 = 0;
+                pc.t1 = nt;
+                pc.slot = 0;
+                pc.nslots = 1;
+                break;
+            }
+        }
+        pc.len = a.seq_lens[pc.b];
+        return true;
     }
-    it.b = lo;
-    it.chunk = rest - prefix[lo];
-    it.nchunks = prefix[lo + 1] - prefix[lo];
-    it.h = hh / nsub;
-    it.hsub = hh - it.h * nsub;
-    int L = a.seq_lens[it.b];
-    if (L < 0 || L > a.max_seq_len || (int64_t)L > (int64_t)a.max_blocks * a.block_size) L = 0;
-    it.len = L;
-    return it;
+};
+
+__device__ __forceinline__ bool len_ok(int L, const DecodeArgs& a)
+{
+    return L >= 0 && L <= a.max_seq_len && (int64_t)L <= (int64_t)a.max_blocks * a.block_size;
 }
 
 template <bool kBF16, int kD, int kGT>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ DecodeArgs a,
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(const __grid_constant__ DecodeArgs a,
                                                                 const int stages)
 {
-    const int chunk_tiles = a.chunk_tiles;
     using T = Traits<kBF16, kD, kGT>;
     extern __shared__ __align__(1024) unsigned char smem[];
     const SharedLayout SL = shared_layout<kBF16, kD, kGT>(stages, a.batch);
     unsigned char* ring = smem + SL.ring_off;
     float* merge = reinterpret_cast<float*>(smem + SL.merge_off);
-    float* pbuf_all = reinterpret_cast<float*>(smem + SL.pbuf_off);
     int* prefix = reinterpret_cast<int*>(smem + SL.prefix_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SL.bar_off);
     uint64_t* empty = full + stages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL.flag_off);
+    int* max_nt_sh = reinterpret_cast<int*>(smem + SL.flag_off + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = a.hq / a.hkv;
     const int nsub = G / kGT;
-    const int heads_x_sub = a.hkv * nsub;
+    const int HH = a.hkv * nsub;  // segments per sequence
 
-    // ---- per-sequence chunk counts and their exclusive prefix sum
+    // ---- tiles per segment of each sequence, prefix sum over the batch
     for (int b = tid; b < a.batch; b += kThreads) {
-        int L = a.seq_lens[b];
-        if (L < 0 || L > a.max_seq_len || (int64_t)L > (int64_t)a.max_blocks * a.block_size) {
-            record_error(a.status, KVATTN_ERR_BAD_INDEX);
-            L = 0;
-        }
-        const int nt = (L + kTile - 1) / kTile;
-        prefix[b + 1] = max(1, (nt + chunk_tiles - 1) / chunk_tiles);
+        const int L = a.seq_lens[b];
+        int nt = 0;
+        if (len_ok(L, a)) nt = (L + kTile - 1) / kTile;
+        else if (blockIdx.x == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
+        prefix[b + 1] = nt;
     }
     if (tid == 0) {
         prefix[0] = 0;
@@ -220,48 +258,91 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == 0) {  // inclusive scan of prefix[1..batch] by one warp
+    if (warp == 0) {  // prefix[i] <- HH * (tiles of sequences 0..i-1); max tiles of one sequence
         const int per = (a.batch + 31) / 32;
         const int beg = 1 + lane * per, end = min(a.batch + 1, beg + per);
-        int s = 0;
-        for (int i = beg; i < end; ++i) s += prefix[i];
+        int s = 0, mx = 0;
+        for (int i = beg; i < end; ++i) {
+            s += prefix[i];
+            mx = max(mx, prefix[i]);
+        }
         int incl = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
         int run = incl - s;
         for (int i = beg; i < end; ++i) {
             run += prefix[i];
-            prefix[i] = run;
+            prefix[i] = run * HH;
         }
+        if (lane == 0) *max_nt_sh = mx;
     }
     __syncthreads();
-    const int num_items = prefix[a.batch] * heads_x_sub;
+
+    // ---- sequences with no keys (or an invalid length): zero output
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+        if (prefix[b + 1] != prefix[b]) continue;
+        for (int e = tid; e < a.hq * kD; e += kThreads) {
+            const int64_t o = (int64_t)b * a.hq * kD + e;
+            if constexpr (kBF16) reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(0.f);
+            else reinterpret_cast<float*>(a.out)[o] = 0.f;
+        }
+        if (a.nslots)
+            for (int h = tid; h < HH; h += kThreads) a.nslots[(int64_t)b * HH + h] = 1;
+    }
+
+    PieceIter iter;
+    iter.P = prefix;
+    iter.batch = a.batch;
+    iter.hh_count = HH;
+    iter.b = 0;
+    iter.flat = a.splits > 1;
+    {
+        const int total = prefix[a.batch];
+        const int max_nt = *max_nt_sh;
+        int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+        if (iter.flat) per = max(per, (max_nt + a.splits - 2) / (a.splits - 1));
+        per = max(per, kMinPer);
+        iter.per = per;
+        iter.r = min(total, (int)blockIdx.x * per);
+        iter.r1 = min(total, iter.r + per);
+        if (iter.flat && iter.r < iter.r1) {  // first sequence of the range
+            int lo = 0, hi = a.batch - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (prefix[mid + 1] > iter.r) hi = mid; else lo = mid + 1;
+            }
+            iter.b = lo;
+        }
+        iter.seg = blockIdx.x;
+    }
 
     if (warp == kConsumerWarps) {
         // =========================== producer warp ===========================
         const uint64_t policy = l2_evict_first_policy();
         uint32_t pos = 0;  // stream position (tiles issued by this CTA)
-        for (int idx = blockIdx.x; idx < num_items; idx += gridDim.x) {
-            ItemInfo it = decode_item(idx, prefix, a.batch, heads_x_sub, nsub, a);
-            const int nt = (it.len + kTile - 1) / kTile;
-            const int t0 = it.chunk * chunk_tiles;
-            const int t1 = min(nt, t0 + chunk_tiles);
-            for (int base = t0; base < t1; base += 32) {
-                // block ids of the next 32 tiles, one coalesced load
-                const int ti = base + lane;
-                int64_t blk = 0;
-                bool ok = true;
-                if (ti < t1) {
-                    const int tok = ti * kTile;
-                    const int32_t v = a.block_table[(int64_t)it.b * a.max_blocks + tok / a.block_size];
-                    ok = v >= 0 && v < a.num_blocks;
-                    blk = ok ? v : 0;
+        Piece pc;
+        while (iter.next(pc, a)) {
+            const int h = pc.hh / nsub;
+            const int32_t* trow = a.block_table + (int64_t)pc.b * a.max_blocks;
+            // block id of tile t (one lane per tile, 32 at a time, next batch prefetched)
+            auto fetch = [&](int t) -> int64_t {
+                if (t >= pc.t1) return 0;
+                const int32_t v = trow[(t * kTile) / a.block_size];
+                if (v < 0 || v >= a.num_blocks) {
+                    record_error(a.status, KVATTN_ERR_BAD_INDEX);
+                    return 0;
                 }
-                if (!ok) record_error(a.status, KVATTN_ERR_BAD_INDEX);
-                const int cnt = min(32, t1 - base);
+                return v;
+            };
+            int64_t blk_next = fetch(pc.t0 + lane);
+            for (int base = pc.t0; base < pc.t1; base += 32) {
+                const int64_t blk = blk_next;
+                if (base + 32 < pc.t1) blk_next = fetch(base + 32 + lane);
+                const int cnt = min(32, pc.t1 - base);
                 for (int j = 0; j < cnt; ++j) {
                     const int64_t bj = __shfl_sync(0xffffffffu, blk, j);
                     if (lane == 0) {
@@ -272,9 +353,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                             *abort_flag = 1;
                         } else {
                             const int tok = (base + j) * kTile;
-                            const int nvalid = min(kTile, it.len - tok);
+                            const int nvalid = min(kTile, pc.len - tok);
                             const uint32_t bytes = (uint32_t)nvalid * kD * T::kE;
-                            const int64_t row = (bj * a.hkv + it.h) * a.block_size + tok % a.block_size;
+                            const int64_t row = (bj * a.hkv + h) * a.block_size + tok % a.block_size;
                             const char* ksrc = (const char*)a.k_pool + row * kD * T::kE;
                             const char* vsrc = (const char*)a.v_pool + row * kD * T::kE;
                             unsigned char* dst = ring + (size_t)stage * T::kStageBytes;
@@ -298,23 +379,23 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
     // ============================== consumer warps ==============================
     const int grp = lane / T::kLPG;      // token group inside the warp
     const int sub = lane % T::kLPG;      // lane inside the group
-    float* pbuf = pbuf_all + warp * T::kTG * T::kV + grp * T::kV;
+    const int M = T::mask(sub);          // XOR layout of this lane's partial scores
+    const int hm = M / T::kTPG, tm = M % T::kTPG;
+    float2* pbuf = reinterpret_cast<float2*>(merge + (size_t)warp * kGT * (kD + 2)) + grp * T::kV;
     const int hq = a.hq;
     uint32_t pos = 0;
+    Piece pc;
 
-    for (int idx = blockIdx.x; idx < num_items; idx += gridDim.x) {
-        ItemInfo it = decode_item(idx, prefix, a.batch, heads_x_sub, nsub, a);
-        const int nt = (it.len + kTile - 1) / kTile;
-        const int t0 = it.chunk * chunk_tiles;
-        const int t1 = min(nt, t0 + chunk_tiles);
-        const int ntiles = max(0, t1 - t0);
-        const int qh0 = it.h * G + it.hsub * kGT;  // first query head of this item
+    while (iter.next(pc, a)) {
+        const int h = pc.hh / nsub, hsub = pc.hh - h * nsub;
+        const int ntiles = pc.t1 - pc.t0;
+        const int qh0 = h * G + hsub * kGT;  // first query head of this segment
 
-        // query slice of this lane, pre-scaled by scale*log2(e)
+        // query slice of this lane (head g^hm in slot g), pre-scaled by scale*log2(e)
         uint64_t q2[kGT][T::kP];
 #pragma unroll
         for (int g = 0; g < kGT; ++g) {
-            const char* qrow = (const char*)a.q + ((int64_t)it.b * hq + qh0 + g) * kD * T::kE;
+            const char* qrow = (const char*)a.q + ((int64_t)pc.b * hq + qh0 + (g ^ hm)) * kD * T::kE;
 #pragma unroll
             for (int c = 0; c < T::kNC; ++c) {
                 const int e0 = c * T::kLPG * T::kCE + sub * T::kCE;
@@ -335,6 +416,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < T::kP; ++i) acc[g][i] = 0;
         }
+        const int my_g = M / T::kTPG;  // the one head whose scores this lane ends up with
 
         for (int li = 0; li < ntiles; ++li) {
             const uint32_t p = pos + li;
@@ -349,14 +431,14 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             }
             const unsigned char* ks = ring + (size_t)stage * T::kStageBytes;
             const unsigned char* vs = ks + T::kTileBytes;
-            const int tok0 = (t0 + li) * kTile;
-            const int nvalid = min(kTile, it.len - tok0);
+            const int tok0 = (pc.t0 + li) * kTile;
+            const int nvalid = min(kTile, pc.len - tok0);
 
-            // ---- partial scores of this lane's tokens and heads
+            // ---- partial scores, slot (g, t) holding head g^hm, token t^tm
             float sc[T::kV];
 #pragma unroll
             for (int t = 0; t < T::kTPG; ++t) {
-                const int row = grp * T::kTPG + t;
+                const int row = grp * T::kTPG + (t ^ tm);
                 uint64_t k2[T::kP];
 #pragma unroll
                 for (int c = 0; c < T::kNC; ++c) {
@@ -372,32 +454,27 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                     sc[g * T::kTPG + t] = pk_lo(s2) + pk_hi(s2);
                 }
             }
-            Bfly<T::kV, T::kLPG / 2>::run(sc, lane);
+            Bfly<T::kV, T::kLPG / 2>::run(sc);
 
-            // ---- scores held by this lane: mask, group max per head
-            float bmax = -INFINITY;  // max of this lane's scores (all belong to one head)
-            int my_g;
+            // ---- this lane's scores (logical index M + r): mask, group max
+            float bmax = -INFINITY;
 #pragma unroll
             for (int r = 0; r < T::kR; ++r) {
-                const int idxv = T::kV >= T::kLPG ? sub * T::kR + r : sub / T::kDup;
-                const int tt = idxv % T::kTPG;
-                my_g = idxv / T::kTPG;
+                const int tt = (M + r) % T::kTPG;
                 if (grp * T::kTPG + tt >= nvalid) sc[r] = -INFINITY;
                 bmax = fmaxf(bmax, sc[r]);
             }
 #pragma unroll
             for (int o = T::kBW / 2; o >= 1; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
-            // every lane of the group learns the tile max of every head
             float mnew[kGT], alpha[kGT];
             bool grow = false;
 #pragma unroll
             for (int g = 0; g < kGT; ++g) {
-                const float tm = __shfl_sync(0xffffffffu, bmax, grp * T::kLPG + g * T::kBW);
-                mnew[g] = fmaxf(m[g], tm);
+                const float tmx = __shfl_sync(0xffffffffu, bmax, grp * T::kLPG + g * T::kBW);
+                mnew[g] = fmaxf(m[g], tmx);
                 alpha[g] = (mnew[g] == -INFINITY) ? 1.f : exp2f(m[g] - mnew[g]);
                 grow |= mnew[g] != m[g];
             }
-            // probabilities of this lane's scores
             float mine_m = mnew[0];
 #pragma unroll
             for (int g = 1; g < kGT; ++g)
@@ -423,14 +500,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                     for (int i = 0; i < T::kP; ++i) acc[g][i] = fmul2(acc[g][i], a2);
                 }
             }
-            // ---- share probabilities inside the group
+            // ---- share probabilities inside the group, as (p, p) pairs
 #pragma unroll
-            for (int r = 0; r < T::kR; ++r) {
-                const int idxv = T::kV >= T::kLPG ? sub * T::kR + r : sub / T::kDup;
-                pbuf[idxv] = sc[r];
-            }
+            for (int r = 0; r < T::kR; ++r) pbuf[M + r] = make_float2(sc[r], sc[r]);
             __syncwarp();
             // ---- weighted V
+            const uint64_t* pb2 = reinterpret_cast<const uint64_t*>(pbuf);
 #pragma unroll
             for (int t = 0; t < T::kTPG; ++t) {
                 const int row = grp * T::kTPG + t;
@@ -444,8 +519,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                     }
 #pragma unroll
                     for (int g = 0; g < kGT; ++g) {
-                        const float pw = pbuf[g * T::kTPG + t];
-                        const uint64_t p2 = pk(pw, pw);
+                        const uint64_t p2 = pb2[g * T::kTPG + t];   // (p, p)
 #pragma unroll
                         for (int i = 0; i < T::kP; ++i) acc[g][i] = ffma2(p2, v2[i], acc[g][i]);
                     }
@@ -462,10 +536,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             float l = lsum[g];
 #pragma unroll
             for (int o = T::kLPG / 2; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-            float M = m[g];
+            float Mx = m[g];
 #pragma unroll
-            for (int o = T::kLPG; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float f = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - M);
+            for (int o = T::kLPG; o < 32; o <<= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+            const float f = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - Mx);
             l *= f;
             const uint64_t f2 = pk(f, f);
 #pragma unroll
@@ -474,15 +548,13 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             for (int o = T::kLPG; o < 32; o <<= 1) {
                 l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-                for (int i = 0; i < T::kP; ++i) {
-                    const uint64_t other = __shfl_xor_sync(0xffffffffu, acc[g][i], o);
-                    acc[g][i] = pk(pk_lo(acc[g][i]) + pk_lo(other), pk_hi(acc[g][i]) + pk_hi(other));
-                }
+                for (int i = 0; i < T::kP; ++i) acc[g][i] = fadd2(acc[g][i], __shfl_xor_sync(0xffffffffu, acc[g][i], o));
             }
-            m[g] = M;
+            m[g] = Mx;
             lsum[g] = l;
         }
-        // ---- write this warp's state, merge the warps
+        // ---- write this warp's state (over its own probability buffer), merge the warps
+        __syncwarp();
         float* mw = merge + (size_t)warp * kGT * (kD + 2);
         if (grp == 0) {
 #pragma unroll
@@ -504,34 +576,35 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        const bool direct = it.nchunks == 1;
+        const bool direct = pc.nslots == 1;
+        if (tid == 0 && pc.slot == 0 && a.nslots) a.nslots[(int64_t)pc.b * HH + pc.hh] = pc.nslots;
         for (int e = tid; e < kGT * kD; e += kConsumerWarps * 32) {
             const int g = e / kD, d = e - g * kD;
-            float M = -INFINITY;
+            float Mx = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[(w * kGT + g) * (kD + 2) + kD]);
+            for (int w = 0; w < kConsumerWarps; ++w) Mx = fmaxf(Mx, merge[(w * kGT + g) * (kD + 2) + kD]);
             float num = 0.f, den = 0.f;
-            if (M != -INFINITY) {
+            if (Mx != -INFINITY) {
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) {
                     const float* mr = merge + (size_t)(w * kGT + g) * (kD + 2);
-                    const float f = (mr[kD] == -INFINITY) ? 0.f : exp2f(mr[kD] - M);
+                    const float f = (mr[kD] == -INFINITY) ? 0.f : exp2f(mr[kD] - Mx);
                     num += f * mr[d];
                     den += f * mr[kD + 1];
                 }
             }
             const float o = den > 0.f ? num / den : 0.f;
-            const int64_t qrow = (int64_t)it.b * hq + qh0 + g;
+            const int64_t qrow = (int64_t)pc.b * hq + qh0 + g;
             if (direct) {
                 if constexpr (kBF16)
                     reinterpret_cast<__nv_bfloat16*>(a.out)[qrow * kD + d] = __float2bfloat16_rn(o);
                 else
                     reinterpret_cast<float*>(a.out)[qrow * kD + d] = o;
             } else {
-                const int64_t prow = qrow * a.splits + it.chunk;
+                const int64_t prow = qrow * a.splits + pc.slot;
                 a.part_o[prow * kD + d] = o;
                 if (d == 0) {
-                    a.part_ml[prow * 2] = M;
+                    a.part_ml[prow * 2] = Mx;
                     a.part_ml[prow * 2 + 1] = den;
                 }
             }
@@ -540,29 +613,27 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
     }
 }
 
-// Merge the chunk partials of the sequences that have more than one chunk.
+// Merge the partial slots of the segments that were cut into several pieces.
 template <bool kBF16, int kD>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeArgs a)
+__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeArgs a, const int gt)
 {
-    const int chunk_tiles = a.chunk_tiles;
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (wid >= a.batch * a.hq) return;
-    const int b = wid / a.hq;
-    int L = a.seq_lens[b];
-    if (L < 0 || L > a.max_seq_len || (int64_t)L > (int64_t)a.max_blocks * a.block_size) L = 0;
-    const int nt = (L + kTile - 1) / kTile;
-    const int nc = max(1, (nt + chunk_tiles - 1) / chunk_tiles);
-    if (nc == 1) return;
+    const int b = wid / a.hq, qh = wid - b * a.hq;
+    const int G = a.hq / a.hkv, nsub = G / gt;
+    const int hh = (qh / G) * nsub + (qh % G) / gt;
+    const int ns = a.nslots[(int64_t)b * a.hkv * nsub + hh];
+    if (ns <= 1) return;
     constexpr int kDL = kD / 32;
     const float* ml = a.part_ml + (int64_t)wid * a.splits * 2;
     float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, ml[2 * c]);
+    for (int c = 0; c < ns; ++c) M = fmaxf(M, ml[2 * c]);
     float acc[kDL];
 #pragma unroll
     for (int i = 0; i < kDL; ++i) acc[i] = 0.f;
     float den = 0.f;
     if (M != -INFINITY) {
-        for (int c = 0; c < nc; ++c) {
+        for (int c = 0; c < ns; ++c) {
             const float mc = ml[2 * c], lc = ml[2 * c + 1];
             const float w = (mc == -INFINITY) ? 0.f : lc * exp2f(mc - M);
             den += w;
@@ -582,17 +653,29 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     }
 }
 
-struct LaunchCfg {
-    int stages = 0, ctas_per_sm = 0, smem = 0;
-};
-
 template <bool kBF16, int kD, int kGT>
 kvattn_status run(const DecodeArgs& a, cudaStream_t s)
 {
-    const int chunk_tiles = a.chunk_tiles;
     using T = Traits<kBF16, kD, kGT>;
-    // ring depth: about 64 KB of stages per CTA
-    const int stages = std::max(4, std::min(16, 65536 / T::kStageBytes));
+    // Ring depth: as many stages (up to 64 KB of them) as leave room for
+    // kCtasPerSm CTAs per SM, counting the per-block reserved shared memory.
+    static int smem_sm = 0, smem_reserved = 0;
+    if (!smem_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+            return KVATTN_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            smem_reserved = 1024;
+    }
+    // The depth must be a multiple of the consumer-warp count: then stage s is
+    // always consumed by warp s % kConsumerWarps, in order, which keeps every
+    // mbarrier wait at most one phase away from the phase it names (parity
+    // waits cannot tell phase u from phase u - 2).
+    const int fixed = shared_layout<kBF16, kD, kGT>(0, a.batch).bytes;
+    const int budget = smem_sm / kCtasPerSm - smem_reserved - fixed;
+    int stages = std::min(65536 / T::kStageBytes, budget / T::kStageBytes);
+    stages = std::max(kConsumerWarps, stages / kConsumerWarps * kConsumerWarps);
     const SharedLayout SL = shared_layout<kBF16, kD, kGT>(stages, a.batch);
     auto kern = decode_split_kernel<kBF16, kD, kGT>;
     static std::mutex mu;
@@ -609,20 +692,13 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, SL.bytes) != cudaSuccess)
         return KVATTN_ERR_CUDA;
     per_sm = std::max(1, per_sm);
-    const int G = a.hq / a.hkv;
-    int64_t items_upper = 0;
-    {
-        const int max_tiles = (a.max_seq_len + kTile - 1) / kTile;
-        const int max_chunks = std::max(1, (max_tiles + chunk_tiles - 1) / chunk_tiles);
-        items_upper = (int64_t)a.batch * max_chunks * a.hkv * (G / kGT);
-    }
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(items_upper, (int64_t)num_sms() * per_sm));
-    kern<<<(unsigned)grid, kThreads, SL.bytes, s>>>(a, stages);
+    const int grid = num_sms() * per_sm;
+    kern<<<grid, kThreads, SL.bytes, s>>>(a, stages);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return KVATTN_ERR_CUDA;
     if (a.splits > 1) {
         const int warps = a.batch * a.hq;
-        decode_combine_kernel<kBF16, kD><<<(warps + 3) / 4, 128, 0, s>>>(a);
+        decode_combine_kernel<kBF16, kD><<<(warps + 3) / 4, 128, 0, s>>>(a, kGT);
         e = cudaGetLastError();
     }
     return cuda_status(e);
@@ -632,24 +708,25 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
 
 DecodePlan decode_plan(int32_t batch, int32_t hkv, int32_t group, int32_t max_seq_len, int32_t splits)
 {
-    const int max_tiles = std::max(1, (max_seq_len + kTile - 1) / kTile);
-    int chunk;
-    if (splits > 0) {
-        chunk = (max_tiles + splits - 1) / splits;
-    } else {
-        // Enough equal-sized chunks for every CTA slot to receive ~16 of them
-        // (static round-robin then balances to a few percent), but at least 8
-        // tiles per chunk so the fixed cost of a chunk stays small.
-        const int nsub = group > 4 ? group / 4 : 1;
-        const int64_t slots = (int64_t)num_sms() * 2;
-        const int64_t pairs = (int64_t)batch * hkv * nsub;
-        const double avg_tiles = std::max(1.0, max_tiles * 0.5);
-        chunk = (int)std::floor(pairs * avg_tiles / (16.0 * slots));
-        chunk = std::max(8, std::min(chunk, max_tiles));
-    }
     DecodePlan p;
-    p.chunk_tiles = std::max(1, chunk);
-    p.max_chunks = (max_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+    const int max_tiles = std::max(1, (max_seq_len + kTile - 1) / kTile);
+    if (splits > 0) {
+        p.slots = splits;
+    } else {
+        // Flat decomposition with at most `slots` pieces per segment: a CTA
+        // range holds ceil(total / grid) tiles, and the piece cap forces at
+        // least ceil(max_tiles / (slots - 1)) per range.  With lengths spread
+        // up to max_seq_len the total is about batch*segments*max_tiles/2, so
+        // slots - 1 >= 4 * grid / (batch * segments) keeps the cap inactive
+        // with a factor-2 margin.
+        const int nsub = group > 4 ? group / 4 : 1;
+        const int64_t segs = std::max<int64_t>(1, (int64_t)batch * hkv * nsub);
+        const int64_t grid = (int64_t)num_sms() * 3;
+        const int64_t want = 1 + (4 * grid + segs - 1) / segs;
+        p.slots = (int32_t)std::max<int64_t>(3, std::min<int64_t>(16, want));
+    }
+    p.slots = std::min(p.slots, max_tiles + 1);
+    if (p.slots < 1) p.slots = 1;
     return p;
 }
 

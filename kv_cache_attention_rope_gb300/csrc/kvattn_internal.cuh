@@ -54,6 +54,7 @@ struct DecodeArgs {
     const int32_t* block_table;
     const int32_t* seq_lens;
     void* out;
+    int32_t* nslots;   // [batch][segments]: pieces each segment was cut into
     float* part_o;     // [batch][hq][splits][d]
     float* part_ml;    // [batch][hq][splits][2] (max in log2 units, sum)
     int64_t num_blocks;
@@ -61,8 +62,7 @@ struct DecodeArgs {
     int32_t max_blocks;
     int32_t batch;
     int32_t max_seq_len;
-    int32_t splits;       // partial slots per (sequence, head) = plan.max_chunks
-    int32_t chunk_tiles;  // 16-token tiles per chunk
+    int32_t splits;    // most pieces per segment (plan.slots); 1 = whole segments
     int32_t hq, hkv, d;
     int32_t dtype;
     float scale_log2;  // softmax scale * log2(e)
@@ -70,14 +70,20 @@ struct DecodeArgs {
 };
 kvattn_status launch_decode(const DecodeArgs& a, cudaStream_t s);
 
-// How the keys of each sequence are cut into chunks: chunks of chunk_tiles
-// 16-token tiles, at most max_chunks per sequence.  splits > 0 asks for at
-// most `splits` chunks of the longest sequence; 0 lets the library choose.
+// Most pieces a (sequence, KV head) segment may be cut into.  splits > 0 is
+// the caller's cap; 0 lets the library choose.  1 = every segment whole.
 struct DecodePlan {
-    int32_t chunk_tiles;
-    int32_t max_chunks;
+    int32_t slots;
 };
 DecodePlan decode_plan(int32_t batch, int32_t hkv, int32_t group, int32_t max_seq_len, int32_t splits);
+
+// Segments per sequence: KV heads, times 2 when a GQA group of 8 is split
+// into two kernels' worth of 4 query heads.
+inline int32_t decode_segments(int32_t hq, int32_t hkv)
+{
+    const int32_t g = hq / hkv;
+    return hkv * (g > 4 ? g / 4 : 1);
+}
 
 struct PrefillArgs {
     const void* q;

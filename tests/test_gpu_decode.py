@@ -212,3 +212,16 @@ def test_c3_full_size_sampled_rows(kvattn_lib):
     _, out = case.run()
     assert kvattn_lib.get_device_status() == 0
     _check(case, out, "c3 full")
+
+
+def test_large_batch_short_sequences(kvattn_lib):
+    """6000 sequences: the per-batch prefix array takes ~24 KB of shared memory,
+    so the kernel runs with a shallower ring (a multiple of the consumer warps);
+    checked on a sample of rows."""
+    wl = workloads.Workload("lb", "large batch", "bf16", 32, 8, 128, "paged", 16, 6000, (0, 60))
+    b = workloads.make_batch(wl)
+    rows = list(range(0, 6000, 397))
+    case = DecodeCase(wl, b, rows)
+    _, out = case.run()
+    assert kvattn_lib.get_device_status() == 0
+    _check(case, out, "large batch")
