@@ -1,14 +1,472 @@
-// Chunked-prefill causal attention (tcgen05 / TMEM).  Placeholder until the
-// tensor-core kernel lands: reports UNSUPPORTED.
-#include "kvattn_internal.cuh"
+// Chunked-prefill causal attention on the tcgen05 tensor cores.
+//
+// What it computes ("From-scratch AI inference engine" page, sections 3.1,
+// 3.3 and 3.4): for chunk c with prefix P (tokens already cached before the
+// chunk) and query row r of the chunk at absolute position P + r,
+//     out[r] = softmax_{k <= P + r}(q[r] . K[k] * scale) V[k]
+// over the keys of the chunk's sequence in the paged cache, which already
+// holds the chunk's own keys.  The online softmax (running max and sum, the
+// accumulated output rescaled when the max grows) tiles the key axis.
+//
+// How (GB300 design), one CTA per (chunk, 128-row query tile, query head):
+//  - warp 0 (one lane) streams with TMA tensor copies: the 128 x 128 bf16 Q
+//    tile once, then 128-key K and V tiles, each gathered as eight 16-token
+//    pages of the KV head straight from the block table, into a two-stage
+//    ring, 128-byte swizzled (the layout the MMA reads).
+//  - warp 1 (one lane) issues the MMAs: S = Q K^T (M = N = 128, K = 128) into
+//    one of two TMEM accumulators, and O += P V (V as an MN-major operand)
+//    into a third; completion is signalled with tcgen05.commit on mbarriers.
+//  - warps 2-5 own one query row per thread (= TMEM lane): load the row of S
+//    from TMEM, apply the causal mask on diagonal tiles, keep the running max
+//    (raised only when it grows by more than 2^8, which bounds p by 256 and
+//    keeps the O rescale rare), write P as bf16 into shared memory for the
+//    next MMA, and finally read O, divide by the row sum and store bf16.
+//  - S of tile t+1 is computed while the softmax works on tile t.
+//  - Every wait is bounded (1 s): a timeout records KVATTN_ERR_TIMEOUT, the
+//    roles stop waiting, drain their in-flight copies and MMAs, free TMEM and
+//    return.
+#include <cstring>
+#include <mutex>
+
+#include "kvattn_tc.cuh"
 
 namespace kvattn {
+namespace {
+
+constexpr int kBM = 128;      // query rows per CTA
+constexpr int kBN = 128;      // keys per KV tile
+constexpr int kHD = 128;      // head dim
+constexpr int kPage = 16;     // tokens per TMA copy of one block
+constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+
+constexpr int kTileBytes = kBM * kHD * 2;  // 32 KB: Q, a K stage, a V stage or P
+constexpr int kPanel = kTileBytes / 2;     // 16 KB: 128 rows x 64 columns
+constexpr int kOffQ = 0;
+constexpr int kOffK = kTileBytes;
+constexpr int kOffV = 3 * kTileBytes;
+constexpr int kOffP = 5 * kTileBytes;
+constexpr int kOffBar = 6 * kTileBytes;
+constexpr int kNumBars = 16;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack to align the base to 1 KB
+
+struct Maps {
+    CUtensorMap q;  // 3-D: (D, Hq, total_q), box (64, 1, 128)
+    CUtensorMap k;  // 2-D: (D, num_blocks * Hkv * block_size), box (64, 16)
+    CUtensorMap v;
+};
+
+struct Bars {
+    uint64_t* q_full;
+    uint64_t* k_full;   // [2]
+    uint64_t* k_empty;  // [2]
+    uint64_t* v_full;   // [2]
+    uint64_t* v_empty;  // [2]
+    uint64_t* s_full;   // [2]
+    uint64_t* s_free;   // [2]
+    uint64_t* p_full;
+    uint64_t* pv_done;
+    uint64_t* drain;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status)
+{
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, status)) return true;
+    *abort_flag = 1;
+    return false;
+}
+
+// Whole-warp wait: every lane waits, the warp agrees (tcgen05.ld/st that
+// follow are warp-collective, so a partial warp must never reach them).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status)
+{
+    const bool ok = wait_or_abort(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ Maps maps, const int n_qt)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    Bars B{bar + 0, bar + 1, bar + 3, bar + 5, bar + 7, bar + 9, bar + 11, bar + 13, bar + 14, bar + 15};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int idx = blockIdx.x;
+    const int j = idx % a.hq;  // query head
+    idx /= a.hq;
+    const int qt = idx % n_qt;  // query tile of the chunk
+    const int c = idx / n_qt;   // chunk
+    const int q0 = a.cu_q_lens[c];
+    const int qlen = a.cu_q_lens[c + 1] - q0;
+    const int P = a.prefix_lens[c];
+    if (qt * kBM >= qlen) return;  // the whole CTA: nothing to do
+    const int seq_len = P + qlen;
+    if (qlen < 0 || P < 0 || qlen > a.max_q_len || q0 < 0 || q0 + qlen > a.total_q ||
+        (int64_t)seq_len > (int64_t)a.max_blocks * a.block_size) {
+        if (threadIdx.x == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
+        return;
+    }
+    const int rows = min(kBM, qlen - qt * kBM);
+    const int pos0 = P + qt * kBM;           // absolute position of query row 0
+    const int n_kv = (pos0 + rows - 1) / kBN + 1;
+    const int h = j / (a.hq / a.hkv);        // KV head
+
+    if (threadIdx.x == 0) {
+        mbar_init(B.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&B.k_full[s], 1);
+            mbar_init(&B.k_empty[s], 1);
+            mbar_init(&B.v_full[s], 1);
+            mbar_init(&B.v_empty[s], 1);
+            mbar_init(&B.s_full[s], 1);
+            mbar_init(&B.s_free[s], 128);
+        }
+        mbar_init(B.p_full, 128);
+        mbar_init(B.pv_done, 1);
+        mbar_init(B.drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tO = tmem + 256;
+
+    if (warp == 0) {
+        // ================================ TMA producer ================================
+        const uint64_t pol_q = l2_evict_first_policy();
+        const uint64_t pol_kv = l2_evict_normal_policy();
+        int issued = 0;  // KV tiles armed
+        if (lane == 0) {
+            tma_prefetch_map(&maps.q);
+            tma_prefetch_map(&maps.k);
+            tma_prefetch_map(&maps.v);
+            mbar_arrive_expect_tx(B.q_full, kTileBytes);
+            tma_load_3d(smem + kOffQ, &maps.q, 0, j, q0 + qt * kBM, B.q_full, pol_q);
+            tma_load_3d(smem + kOffQ + kPanel, &maps.q, 64, j, q0 + qt * kBM, B.q_full, pol_q);
+        }
+        const int32_t* trow = a.block_table + (int64_t)c * a.max_blocks;
+        for (int t = 0; t < n_kv; ++t) {
+            const int stage = t & 1;
+            // lane g < 8: page g of this tile (keys 128t + 16g ..)
+            int y = 0;
+            bool have = false;
+            if (lane < kBN / kPage) {
+                const int key0 = t * kBN + lane * kPage;
+                if (key0 < seq_len) {
+                    const int32_t blk = trow[key0 / a.block_size];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        record_error(a.status, KVATTN_ERR_BAD_INDEX);
+                    } else {
+                        y = (int)(((int64_t)blk * a.hkv + h) * a.block_size + key0 % a.block_size);
+                        have = true;
+                    }
+                }
+            }
+            const unsigned pages = __ballot_sync(0xffffffffu, have);
+            const uint32_t bytes = (uint32_t)__popc(pages) * 2u * (kPage * 128u);
+            bool go = true;
+            if (lane == 0) {
+                if (t >= 2) go = wait_or_abort(&B.k_empty[stage], ((t >> 1) - 1) & 1, abort_flag, a.status);
+                else go = !*abort_flag;
+                if (go) mbar_arrive_expect_tx(&B.k_full[stage], bytes);
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) break;
+            for (int g = 0; g < kBN / kPage; ++g) {
+                const int yg = __shfl_sync(0xffffffffu, y, g);
+                if (lane == 0 && ((pages >> g) & 1u)) {
+                    unsigned char* dst = smem + kOffK + stage * kTileBytes + g * (kPage * 128);
+                    tma_load_2d(dst, &maps.k, 0, yg, &B.k_full[stage], pol_kv);
+                    tma_load_2d(dst + kPanel, &maps.k, 64, yg, &B.k_full[stage], pol_kv);
+                }
+            }
+            if (lane == 0) {
+                if (t >= 2) go = wait_or_abort(&B.v_empty[stage], ((t >> 1) - 1) & 1, abort_flag, a.status);
+                else go = !*abort_flag;
+                if (go) mbar_arrive_expect_tx(&B.v_full[stage], bytes);
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) break;
+            for (int g = 0; g < kBN / kPage; ++g) {
+                const int yg = __shfl_sync(0xffffffffu, y, g);
+                if (lane == 0 && ((pages >> g) & 1u)) {
+                    unsigned char* dst = smem + kOffV + stage * kTileBytes + g * (kPage * 128);
+                    tma_load_2d(dst, &maps.v, 0, yg, &B.v_full[stage], pol_kv);
+                    tma_load_2d(dst + kPanel, &maps.v, 64, yg, &B.v_full[stage], pol_kv);
+                }
+            }
+            issued = t + 1;
+        }
+        // After an abort, let every armed copy land before the CTA can exit.
+        if (lane == 0 && *abort_flag) {
+            for (int t = max(0, issued - 2); t < issued; ++t) {
+                mbar_wait(&B.k_full[t & 1], (t >> 1) & 1, a.status);
+                mbar_wait(&B.v_full[t & 1], (t >> 1) & 1, a.status);
+            }
+            mbar_wait(B.q_full, 0, a.status);
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer =================================
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kHD, true);
+            const uint32_t sQ = smem_addr(smem + kOffQ), sP = smem_addr(smem + kOffP);
+            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status);
+            auto issue_s = [&](int t) -> bool {
+                const int stage = t & 1;
+                if (!wait_or_abort(&B.k_full[stage], (t >> 1) & 1, abort_flag, a.status)) return false;
+                if (t >= 2 && !wait_or_abort(&B.s_free[stage], ((t >> 1) - 1) & 1, abort_flag, a.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t sK = smem_addr(smem + kOffK + stage * kTileBytes);
+#pragma unroll
+                for (int k = 0; k < kHD / 16; ++k) {
+                    const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
+                    tc_mma_f16(tmem + stage * 128, umma_desc_sw128(sQ + off, 16, 1024),
+                               umma_desc_sw128(sK + off, 16, 1024), idesc_s, k > 0);
+                }
+                tc_commit(&B.s_full[stage]);
+                tc_commit(&B.k_empty[stage]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int t = 0; ok && t < n_kv; ++t) {
+                if (t + 1 < n_kv && !issue_s(t + 1)) break;
+                const int stage = t & 1;
+                if (!wait_or_abort(&B.v_full[stage], (t >> 1) & 1, abort_flag, a.status)) break;
+                if (!wait_or_abort(B.p_full, t & 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                const uint32_t sV = smem_addr(smem + kOffV + stage * kTileBytes);
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint32_t offp = (k >> 2) * kPanel + (k & 3) * 32;
+                    tc_mma_f16(tO, umma_desc_sw128(sP + offp, 16, 1024),
+                               umma_desc_sw128(sV + k * 16 * 128, kPanel, 1024), idesc_o, (t > 0 || k > 0));
+                }
+                tc_commit(&B.v_empty[stage]);
+                tc_commit(B.pv_done);
+            }
+            // every MMA this thread issued has completed once `drain` flips
+            tc_commit(B.drain);
+            mbar_wait(B.drain, 0, a.status);
+        }
+    } else {
+        // ============================ softmax / epilogue ============================
+        const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
+        const int r = quarter * 32 + lane;        // query row of this thread
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int pos_r = pos0 + r;
+        const float sl2 = a.scale_log2;
+        float m_used = -INFINITY, lsum = 0.f;
+        bool ok = true;
+        unsigned char* sP = smem + kOffP;
+        for (int t = 0; t < n_kv; ++t) {
+            const int buf = t & 1;
+            if (!warp_wait(&B.s_full[buf], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+            float s[kBN];
+#pragma unroll
+            for (int i = 0; i < kBN / 32; ++i) {
+                uint32_t v[32];
+                tmem_ld32(tmem + buf * 128 + lane_base + i * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[i * 32 + e] = __uint_as_float(v[e]);
+            }
+            tc_fence_before();
+            mbar_arrive(&B.s_free[buf]);
+            // causal mask (only tiles that reach past the first row's position)
+            float mx = -INFINITY;
+            if (t * kBN + kBN - 1 > pos0) {
+                const int lim = pos_r - t * kBN;  // last visible column
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) {
+                    if (i > lim) s[i] = -INFINITY;
+                    mx = fmaxf(mx, s[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+            }
+            const float m_tile = mx * sl2;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (m_used == -INFINITY) {
+                m_used = m_tile;
+            } else if (m_tile > m_used + 8.f) {
+                alpha = exp2f(m_used - m_tile);
+                m_used = m_tile;
+                rescale = true;
+            }
+            // P = exp2(s*scale*log2e - m), bf16, into the swizzled P tile
+            uint32_t pk2[kBN / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < kBN / 2; ++i) {
+                float p0 = (s[2 * i] == -INFINITY || m_used == -INFINITY) ? 0.f
+                                                                          : exp2f(fmaf(s[2 * i], sl2, -m_used));
+                float p1 = (s[2 * i + 1] == -INFINITY || m_used == -INFINITY)
+                               ? 0.f
+                               : exp2f(fmaf(s[2 * i + 1], sl2, -m_used));
+                const uint32_t w = pack_bf16_rn(p0, p1);
+                pk2[i] = w;
+                rs += bf16lo(w) + bf16hi(w);  // sum what the MMA will actually use
+            }
+            lsum = lsum * alpha + rs;
+            if (t > 0 && !warp_wait(B.pv_done, (t - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            // tcgen05.ld/st are warp-collective: the whole warp rescales if
+            // any of its rows must (alpha is 1 for the others)
+            if (__any_sync(0xffffffffu, rescale && t > 0)) {
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < kHD / 32; ++i) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + lane_base + i * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st32(tO + lane_base + i * 32, v);
+                }
+                tmem_st_wait();
+            }
+            // keys past the end of the sequence: V rows must be zero (stale
+            // cache slots may hold anything, and 0 * NaN is NaN)
+            if ((t + 1) * kBN > seq_len) {
+                if (!warp_wait(&B.v_full[buf], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                if (t * kBN + r >= seq_len) {
+                    unsigned char* vrow = smem + kOffV + buf * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                    for (int pnl = 0; pnl < 2; ++pnl)
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            *reinterpret_cast<uint4*>(vrow + pnl * kPanel + ch * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            // row r of P: 2 panels x 8 chunks of 16 bytes, chunk index XOR (r % 8)
+            unsigned char* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int pnl = 0; pnl < 2; ++pnl)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int w0 = pnl * 32 + ch * 4;
+                    *reinterpret_cast<uint4*>(prow + pnl * kPanel + ((ch ^ (r & 7)) << 4)) =
+                        make_uint4(pk2[w0], pk2[w0 + 1], pk2[w0 + 2], pk2[w0 + 3]);
+                }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(B.p_full);
+        }
+        // epilogue: O / l -> bf16 rows of out
+        if (ok && warp_wait(B.pv_done, (n_kv - 1) & 1, abort_flag, a.status)) {
+            tc_fence_after();
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            __nv_bfloat16* orow =
+                reinterpret_cast<__nv_bfloat16*>(a.out) + ((int64_t)(q0 + qt * kBM + r) * a.hq + j) * kHD;
+#pragma unroll
+            for (int i = 0; i < kHD / 32; ++i) {
+                uint32_t v[32];
+                tmem_ld32(tO + lane_base + i * 32, v);
+                tmem_ld_wait();
+                if (r < rows) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = pack_bf16_rn(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                        w.y = pack_bf16_rn(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                        w.z = pack_bf16_rn(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                        w.w = pack_bf16_rn(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + i * 32 + e) = w;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---- host: tensor maps --------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder()
+{
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+bool make_maps(const PrefillArgs& a, Maps& m)
+{
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    std::memset(&m, 0, sizeof(m));
+    const cuuint32_t estr[3] = {1, 1, 1};
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kHD, (cuuint64_t)a.hq, (cuuint64_t)a.total_q};
+        const cuuint64_t strides[2] = {(cuuint64_t)kHD * 2, (cuuint64_t)a.hq * kHD * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
+        if (enc(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.hkv * a.block_size;
+    const cuuint64_t dims[2] = {(cuuint64_t)kHD, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHD * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    if (enc(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.k_pool), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    if (enc(&m.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.v_pool), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    return true;
+}
+
+}  // namespace
 
 kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
 {
-    (void)a;
-    (void)s;
-    return KVATTN_ERR_UNSUPPORTED;
+    if (a.d != kHD || a.hq % a.hkv) return KVATTN_ERR_UNSUPPORTED;
+    if ((int64_t)a.num_blocks * a.hkv * a.block_size >= ((int64_t)1 << 31)) return KVATTN_ERR_UNSUPPORTED;
+    Maps maps;
+    if (!make_maps(a, maps)) return KVATTN_ERR_CUDA;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return KVATTN_ERR_CUDA;
+    const int n_qt = (a.max_q_len + kBM - 1) / kBM;
+    const int64_t grid = (int64_t)a.num_chunks * n_qt * a.hq;
+    if (grid <= 0) return KVATTN_OK;
+    if (grid > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
+    prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, maps, n_qt);
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace kvattn

@@ -157,3 +157,75 @@ class DecodeCase:
         outs = oracle.attend(self.ocache, np.stack(qh), list(range(len(self.rows))), pos, self.o_table,
                              self.wl.num_q_heads)
         return np.stack(qh), outs
+
+
+class PrefillCase:
+    """Chunks of new query tokens over cached prefixes: the chunk tokens go
+    through rope_append (GPU) and rope + round + append (oracle); history
+    tokens before each prefix are drawn N(0,1) and written to both caches."""
+
+    def __init__(self, hq, hkv, prefixes, qlens, block_size=16, seed=0, device="cuda", k_scale=None,
+                 extra_blocks=5):
+        D = 128
+        self.hq, self.hkv, self.D = hq, hkv, D
+        self.prefixes = np.asarray(prefixes, dtype=np.int64)
+        self.qlens = np.asarray(qlens, dtype=np.int64)
+        n = len(prefixes)
+        BS = block_size
+        total = self.prefixes + self.qlens
+        need = (total + BS - 1) // BS
+        nb = int(need.sum()) + extra_blocks
+        g = np.random.default_rng(seed)
+        perm = g.permutation(nb).astype(np.int32)
+        table = np.full((n, int(need.max())), -1, dtype=np.int32)
+        o = 0
+        for r, k in enumerate(need):
+            table[r, :k] = perm[o:o + k]
+            o += k
+        self.table = table
+        self.device = torch.device(device)
+        self.cfg = kv.make_config(hq, hkv, D, kv.BF16)
+        self.cache = kv.Cache.empty(nb, hkv, BS, D, torch.bfloat16, self.device)
+        self.cache.k_pool.fill_(float("nan"))
+        self.cache.v_pool.fill_(float("nan"))
+        self.ocache = oracle.Cache(nb, BS, hkv, D)
+        for r in range(n):
+            P = int(self.prefixes[r])
+            if P:
+                k = torch.from_numpy(g.standard_normal((P, hkv, D), dtype=np.float32)).to(torch.bfloat16)
+                v = torch.from_numpy(g.standard_normal((P, hkv, D), dtype=np.float32)).to(torch.bfloat16)
+                put_rows(self.cache.k_pool, table[r], np.arange(P), k.to(self.device))
+                put_rows(self.cache.v_pool, table[r], np.arange(P), v.to(self.device))
+                oracle.append(self.ocache, k.double().numpy(), v.double().numpy(), np.arange(P),
+                              np.full(P, r, np.int32), table)
+        T = int(self.qlens.sum())
+        self.q_raw = torch.from_numpy(g.standard_normal((T, hq, D), dtype=np.float32)).to(torch.bfloat16)
+        k_raw = g.standard_normal((T, hkv, D), dtype=np.float32)
+        if k_scale is not None:
+            k_raw = k_raw * k_scale(np.arange(T))[:, None, None]
+        self.k_raw = torch.from_numpy(k_raw).to(torch.bfloat16)
+        self.v_raw = torch.from_numpy(g.standard_normal((T, hkv, D), dtype=np.float32)).to(torch.bfloat16)
+        self.pos = np.concatenate([np.arange(p, p + q) for p, q in zip(self.prefixes, self.qlens)]).astype(np.int32)
+        self.seq = np.concatenate([np.full(q, r) for r, q in enumerate(self.qlens)]).astype(np.int32)
+        self.cu = np.zeros(n + 1, dtype=np.int32)
+        self.cu[1:] = np.cumsum(self.qlens)
+
+    def run(self):
+        dev = self.device
+        q = self.q_raw.to(dev).contiguous()
+        d_table = torch.from_numpy(self.table).to(dev)
+        kv.rope_append(self.cfg, self.cache, q, self.k_raw.to(dev), self.v_raw.to(dev),
+                       torch.from_numpy(self.pos).to(dev), torch.from_numpy(self.seq).to(dev), d_table)
+        out = kv.prefill_chunk(self.cfg, self.cache, q, torch.from_numpy(self.cu).to(dev),
+                               torch.from_numpy(self.prefixes.astype(np.int32)).to(dev), d_table,
+                               int(self.qlens.max()))
+        return q, out
+
+    def expected(self, rows=None):
+        """Oracle output for the given query rows (indices into the chunk tokens)."""
+        od = oracle.BF16
+        kh = oracle.round_to(oracle.rope(self.k_raw.double().numpy(), self.pos), od)
+        oracle.append(self.ocache, kh, self.v_raw.double().numpy(), self.pos, self.seq, self.table)
+        rows = np.arange(len(self.pos)) if rows is None else np.asarray(rows)
+        qh = oracle.round_to(oracle.rope(self.q_raw[rows].double().numpy(), self.pos[rows]), od)
+        return rows, oracle.attend(self.ocache, qh, self.seq[rows], self.pos[rows], self.table, self.hq)

@@ -1,0 +1,70 @@
+"""GPU parity of the tcgen05 chunked-prefill kernel against the fp64 oracle.
+
+Tolerance: bf16 output, max abs <= 1e-2 and relative L2 <= 5e-3 against the
+exact attention of the correctly rounded q/k/v.  Pools are NaN-filled, so a
+stale cache slot that leaks into a result fails the test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from _gpu_support import PrefillCase, compare, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(kv, case, rows=None, what="prefill"):
+    _, out = case.run()
+    assert kv.get_device_status() == 0
+    rows, ref = case.expected(rows)
+    return compare(f64(out)[rows], ref, "bf16", what)
+
+
+def test_causal_no_prefix_two_query_tiles(kvattn_lib):
+    _check(kvattn_lib, PrefillCase(4, 2, [0], [200]), what="prefix 0, 200 rows")
+
+
+@pytest.mark.parametrize("prefixes,qlens", [
+    ([300], [130]),                   # prefix not a multiple of 16 / 128
+    ([0, 17, 128, 1000], [1, 128, 129, 64]),   # ragged chunks, one-row chunk
+    ([5, 4096], [512, 3]),
+])
+def test_prefixes_and_ragged_chunks(kvattn_lib, prefixes, qlens):
+    _check(kvattn_lib, PrefillCase(8, 2, prefixes, qlens, seed=len(prefixes)), what=f"{prefixes}/{qlens}")
+
+
+def test_mha_and_block_size_32(kvattn_lib):
+    _check(kvattn_lib, PrefillCase(4, 4, [50, 333], [77, 200], block_size=32, seed=3), what="MHA, BS 32")
+
+
+def test_running_max_rescale(kvattn_lib):
+    """Keys whose scale grows along the sequence push each row's max up by far
+    more than 2^8 from tile to tile, so the accumulated output is rescaled.
+
+    Scores here reach +-16, so a row's softmax is dominated by a few keys and
+    the bf16 rounding of the probabilities fed to the tensor-core P.V product
+    (P must share V's type) does not average out: each normalised weight is off
+    by at most ~2^-8 relative, so |out - exact| <= 2^-8 (max|v| + |exact|).
+    That derived bound replaces the 1e-2 absolute bar, which is stated for the
+    N(0,1) workloads; the relative L2 bar is kept."""
+    kv = kvattn_lib
+    case = PrefillCase(4, 1, [0], [600], seed=4, k_scale=lambda t: 1.0 + t / 40.0)
+    _, out = case.run()
+    assert kv.get_device_status() == 0
+    rows, ref = case.expected()
+    got = f64(out)[rows]
+    vmax = float(case.v_raw.abs().max())
+    bound = 2.0 ** -8 * (vmax + np.abs(ref))
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) - bound))
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-3
+
+
+def test_c5_chunks_sampled_rows(kvattn_lib):
+    """Two chunks of the mixed workload (their prefixes, 512 queries, 32/8 x 128)."""
+    wl = workloads.WORKLOADS["c5"]
+    _, pre = workloads.lengths(wl)
+    idx = [int(np.argmin(pre)), int(np.argmax(pre))]
+    case = PrefillCase(32, 8, [int(pre[i]) for i in idx], [512, 512], seed=5)
+    rows = np.arange(0, 1024, 13)
+    _check(kvattn_lib, case, rows=rows, what="c5 chunks")

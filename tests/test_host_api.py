@@ -114,7 +114,9 @@ def test_decode_plan_properties(kv):
         for s in (1, 2, 3, 7):
             n = kv.decode_num_splits(cfg, 4, maxlen, s)
             assert 1 <= n <= s
-    assert kv.decode_num_splits(cfg, 4, 16, 8) == 1     # one tile cannot be split
+    # a segment cut where two CTA ranges meet has at most (tiles + 1) pieces
+    assert kv.decode_num_splits(cfg, 4, 16, 8) == 2
+    assert kv.decode_num_splits(cfg, 4, 16, 1) == 1     # 1 = whole segments, no workspace
     assert kv.decode_workspace_size(cfg, -1, 10, 0) == 0
     # workspace grows with the batch
     assert kv.decode_workspace_size(cfg, 64, 4096, 4) > kv.decode_workspace_size(cfg, 8, 4096, 4)
