@@ -16,6 +16,7 @@ own GPU (the path shards by sequence; no collective in the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -45,6 +46,8 @@ def parse_args():
     p.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=DEFAULT_WORKLOAD)
     p.add_argument("--rows", type=int, default=0,
                    help="use only the first N decode rows of the workload (profiling small cases)")
+    p.add_argument("--chunks", type=int, default=-1,
+                   help="use only the first N prefill chunks of the workload (profiling small cases)")
     p.add_argument("--compact-pool", action="store_true",
                    help="pool of twice the blocks the batch needs instead of the workload's pool size")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -121,7 +124,7 @@ class ClockSampler:
 class Step:
     """A workload's step on one GPU, inputs resident in HBM."""
 
-    def __init__(self, wl: workloads.Workload, device, rows: int = 0, compact_pool: bool = False):
+    def __init__(self, wl: workloads.Workload, device, rows: int = 0, compact_pool: bool = False, chunks: int = -1):
         import torch
 
         import kv_cache_attention_rope_gb300 as kv
@@ -133,8 +136,13 @@ class Step:
         per_block = 2 * BS * H * D * wl.elem_bytes
         nb = None
         subset = None
-        if rows:
-            subset = list(range(wl.chunks)) + list(range(wl.chunks, min(wl.chunks + rows, wl.chunks + wl.decode_batch)))
+        if rows or chunks >= 0:
+            nc = wl.chunks if chunks < 0 else min(chunks, wl.chunks)
+            nd = wl.decode_batch if not rows else min(rows, wl.decode_batch)
+            if nc != wl.chunks:
+                wl = dataclasses.replace(wl, chunks=nc)
+                self.wl = wl
+            subset = list(range(nc)) + list(range(nc, nc + nd))
         if wl.layout == "paged":
             if compact_pool:
                 probe = workloads.make_batch(wl, num_blocks=1 << 30, rows_subset=subset)
@@ -365,7 +373,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     wl = workloads.WORKLOADS[args.workload]
-    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool)
+    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool, chunks=args.chunks)
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
