@@ -76,6 +76,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     return false;
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz: a few ulp relative
+// error, far below the bf16 rounding P goes through); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Whole-warp wait: every lane waits, the warp agrees (tcgen05.ld/st that
 // follow are warp-collective, so a partial warp must never reach them).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status)
@@ -152,21 +161,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem + kOffQ + kPanel, &maps.q, 64, j, q0 + qt * kBM, B.q_full, pol_q);
         }
         const int32_t* trow = a.block_table + (int64_t)c * a.max_blocks;
+        // lane g < 8 loads the block id of page g of tile t (keys 128t + 16g ..)
+        auto fetch = [&](int t) -> int32_t {
+            const int key0 = t * kBN + lane * kPage;
+            return (lane < kBN / kPage && t < n_kv && key0 < seq_len) ? trow[key0 / a.block_size] : -1;
+        };
+        int32_t blk_next = fetch(0);
         for (int t = 0; t < n_kv; ++t) {
             const int stage = t & 1;
-            // lane g < 8: page g of this tile (keys 128t + 16g ..)
+            const int32_t blk = blk_next;
+            blk_next = fetch(t + 1);  // in flight while this tile is issued
             int y = 0;
             bool have = false;
-            if (lane < kBN / kPage) {
-                const int key0 = t * kBN + lane * kPage;
-                if (key0 < seq_len) {
-                    const int32_t blk = trow[key0 / a.block_size];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        record_error(a.status, KVATTN_ERR_BAD_INDEX);
-                    } else {
-                        y = (int)(((int64_t)blk * a.hkv + h) * a.block_size + key0 % a.block_size);
-                        have = true;
-                    }
+            const int key0 = t * kBN + lane * kPage;
+            if (lane < kBN / kPage && key0 < seq_len) {
+                if (blk < 0 || blk >= a.num_blocks) {
+                    record_error(a.status, KVATTN_ERR_BAD_INDEX);
+                } else {
+                    y = (int)(((int64_t)blk * a.hkv + h) * a.block_size + key0 % a.block_size);
+                    have = true;
                 }
             }
             const unsigned pages = __ballot_sync(0xffffffffu, have);
@@ -271,29 +284,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = t & 1;
             if (!warp_wait(&B.s_full[buf], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
-            float s[kBN];
+            uint32_t sv[kBN];
 #pragma unroll
-            for (int i = 0; i < kBN / 32; ++i) {
-                uint32_t v[32];
-                tmem_ld32(tmem + buf * 128 + lane_base + i * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) s[i * 32 + e] = __uint_as_float(v[e]);
-            }
+            for (int i = 0; i < kBN / 32; ++i)
+                tmem_ld32(tmem + buf * 128 + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[i * 32]));
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&B.s_free[buf]);
-            // causal mask (only tiles that reach past the first row's position)
+            // causal mask: keys past this row's position (only tiles that reach
+            // beyond the first row's position can have any)
+            const int lim = (t * kBN + kBN - 1 > pos0) ? pos_r - t * kBN : kBN - 1;  // last visible column
             float mx = -INFINITY;
-            if (t * kBN + kBN - 1 > pos0) {
-                const int lim = pos_r - t * kBN;  // last visible column
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    if (i > lim) s[i] = -INFINITY;
-                    mx = fmaxf(mx, s[i]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+            for (int i = 0; i < kBN; ++i) {
+                const float x = i <= lim ? __uint_as_float(sv[i]) : -INFINITY;
+                sv[i] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
             }
             const float m_tile = mx * sl2;
             float alpha = 1.f;
@@ -301,24 +307,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (m_used == -INFINITY) {
                 m_used = m_tile;
             } else if (m_tile > m_used + 8.f) {
-                alpha = exp2f(m_used - m_tile);
+                alpha = fast_exp2(m_used - m_tile);
                 m_used = m_tile;
                 rescale = true;
             }
-            // P = exp2(s*scale*log2e - m), bf16, into the swizzled P tile
+            // P = 2^(s*scale*log2e - m) as bf16; a row with no visible key yet
+            // subtracts +inf so every p is 0
+            const float msub = m_used == -INFINITY ? INFINITY : m_used;
             uint32_t pk2[kBN / 2];
-            float rs = 0.f;
+            float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
             for (int i = 0; i < kBN / 2; ++i) {
-                float p0 = (s[2 * i] == -INFINITY || m_used == -INFINITY) ? 0.f
-                                                                          : exp2f(fmaf(s[2 * i], sl2, -m_used));
-                float p1 = (s[2 * i + 1] == -INFINITY || m_used == -INFINITY)
-                               ? 0.f
-                               : exp2f(fmaf(s[2 * i + 1], sl2, -m_used));
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * i]), sl2, -msub));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * i + 1]), sl2, -msub));
                 const uint32_t w = pack_bf16_rn(p0, p1);
                 pk2[i] = w;
-                rs += bf16lo(w) + bf16hi(w);  // sum what the MMA will actually use
+                rs0 += bf16lo(w);  // sum what the MMA will actually use
+                rs1 += bf16hi(w);
             }
+            const float rs = rs0 + rs1;
             lsum = lsum * alpha + rs;
             if (t > 0 && !warp_wait(B.pv_done, (t - 1) & 1, abort_flag, a.status)) { ok = false; break; }
             // tcgen05.ld/st are warp-collective: the whole warp rescales if
