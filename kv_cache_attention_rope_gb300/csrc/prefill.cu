@@ -8,20 +8,24 @@
 // holds the chunk's own keys.  The online softmax (running max and sum, the
 // accumulated output rescaled when the max grows) tiles the key axis.
 //
-// How (GB300 design), one CTA per (chunk, 128-row query tile, query head):
-//  - warp 0 (one lane) streams with TMA tensor copies: the 128 x 128 bf16 Q
-//    tile once, then 128-key K and V tiles, each gathered as eight 16-token
-//    pages of the KV head straight from the block table, into a two-stage
-//    ring, 128-byte swizzled (the layout the MMA reads).
-//  - warp 1 (one lane) issues the MMAs: S = Q K^T (M = N = 128, K = 128) into
-//    one of two TMEM accumulators, and O += P V (V as an MN-major operand)
-//    into a third; completion is signalled with tcgen05.commit on mbarriers.
-//  - warps 2-5 own one query row per thread (= TMEM lane): load the row of S
+// How (GB300 design), one CTA per (chunk, 256 query rows, query head), the
+// rows split into two 128-row tiles A and B that share one K/V stream:
+//  - warp 0 (one lane) streams with TMA tensor copies: both 128 x 128 bf16 Q
+//    tiles once, then 128-key K and V tiles, each gathered as eight 16-token
+//    pages of the KV head straight from the block table (K in one stage, V in
+//    two), 128-byte swizzled (the layout the MMA reads).
+//  - warp 1 (one lane) issues the MMAs: S_x = Q_x K^T (M = N = 128, K = 128)
+//    and O_x += P_x V (V as an MN-major operand), x = A, B, all four
+//    accumulators in TMEM (512 columns); completion is signalled with
+//    tcgen05.commit on mbarriers.  The order S_A S_B | PV_A S_A' PV_B S_B' |
+//    ... keeps the tensor core busy with one tile while the other's softmax
+//    runs (ping-pong).
+//  - warps 2-5 (tile A) and 6-9 (tile B) own one query row per thread
+//    (= TMEM lane): load the row of S
 //    from TMEM, apply the causal mask on diagonal tiles, keep the running max
 //    (raised only when it grows by more than 2^8, which bounds p by 256 and
 //    keeps the O rescale rare), write P as bf16 into shared memory for the
 //    next MMA, and finally read O, divide by the row sum and store bf16.
-//  - S of tile t+1 is computed while the softmax works on tile t.
 //  - Every wait is bounded (1 s): a timeout records KVATTN_ERR_TIMEOUT, the
 //    roles stop waiting, drain their in-flight copies and MMAs, free TMEM and
 //    return.
@@ -33,19 +37,19 @@
 namespace kvattn {
 namespace {
 
-constexpr int kBM = 128;      // query rows per CTA
+constexpr int kBM = 128;      // query rows per tile (two tiles per CTA: A and B)
 constexpr int kBN = 128;      // keys per KV tile
 constexpr int kHD = 128;      // head dim
 constexpr int kPage = 16;     // tokens per TMA copy of one block
-constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 320; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, warps 6-9 softmax B
 
-constexpr int kTileBytes = kBM * kHD * 2;  // 32 KB: Q, a K stage, a V stage or P
+constexpr int kTileBytes = kBM * kHD * 2;  // 32 KB: a Q tile, the K stage, a V stage or a P tile
 constexpr int kPanel = kTileBytes / 2;     // 16 KB: 128 rows x 64 columns
-constexpr int kOffQ = 0;
-constexpr int kOffK = kTileBytes;
-constexpr int kOffV = 3 * kTileBytes;
-constexpr int kOffP = 5 * kTileBytes;
-constexpr int kOffBar = 6 * kTileBytes;
+constexpr int kOffQ = 0;                   // Q_A, Q_B
+constexpr int kOffK = 2 * kTileBytes;      // one stage
+constexpr int kOffV = 3 * kTileBytes;      // two stages
+constexpr int kOffP = 5 * kTileBytes;      // P_A, P_B
+constexpr int kOffBar = 7 * kTileBytes;
 constexpr int kNumBars = 16;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack to align the base to 1 KB
 
@@ -57,14 +61,14 @@ struct Maps {
 
 struct Bars {
     uint64_t* q_full;
-    uint64_t* k_full;   // [2]
-    uint64_t* k_empty;  // [2]
+    uint64_t* k_full;
+    uint64_t* k_empty;
     uint64_t* v_full;   // [2]
     uint64_t* v_empty;  // [2]
-    uint64_t* s_full;   // [2]
+    uint64_t* s_full;   // [2]: tile A, tile B
     uint64_t* s_free;   // [2]
-    uint64_t* p_full;
-    uint64_t* pv_done;
+    uint64_t* p_full;   // [2]
+    uint64_t* pv_done;  // [2]
     uint64_t* drain;
 };
 
@@ -93,13 +97,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// One CTA: query rows [256 qt, 256 qt + 256) of chunk c, head j, as tiles A
+// (first 128 rows) and B (next 128), both against the same K/V stream.  The
+// MMA order S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ... keeps the
+// tensor core on one tile while the other tile's softmax runs.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ Maps maps, const int n_qt)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    Bars B{bar + 0, bar + 1, bar + 3, bar + 5, bar + 7, bar + 9, bar + 11, bar + 13, bar + 14, bar + 15};
+    Bars B{bar + 0, bar + 1, bar + 2, bar + 3, bar + 5, bar + 7, bar + 9, bar + 11, bar + 13, bar + 15};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -107,35 +115,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     int idx = blockIdx.x;
     const int j = idx % a.hq;  // query head
     idx /= a.hq;
-    const int qt = idx % n_qt;  // query tile of the chunk
+    const int qt = idx % n_qt;  // 256-row query block of the chunk
     const int c = idx / n_qt;   // chunk
     const int q0 = a.cu_q_lens[c];
     const int qlen = a.cu_q_lens[c + 1] - q0;
     const int P = a.prefix_lens[c];
-    if (qt * kBM >= qlen) return;  // the whole CTA: nothing to do
+    if (qt * 2 * kBM >= qlen) return;  // the whole CTA: nothing to do
     const int seq_len = P + qlen;
     if (qlen < 0 || P < 0 || qlen > a.max_q_len || q0 < 0 || q0 + qlen > a.total_q ||
         (int64_t)seq_len > (int64_t)a.max_blocks * a.block_size) {
         if (threadIdx.x == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
         return;
     }
-    const int rows = min(kBM, qlen - qt * kBM);
-    const int pos0 = P + qt * kBM;           // absolute position of query row 0
+    const int rows = min(2 * kBM, qlen - qt * 2 * kBM);  // valid rows of the 256
+    const int row0 = q0 + qt * 2 * kBM;                   // first q row (token index)
+    const int pos0 = P + qt * 2 * kBM;                    // absolute position of row 0
     const int n_kv = (pos0 + rows - 1) / kBN + 1;
-    const int h = j / (a.hq / a.hkv);        // KV head
+    const int h = j / (a.hq / a.hkv);  // KV head
 
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 1);
+        mbar_init(B.k_full, 1);
+        mbar_init(B.k_empty, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&B.k_full[s], 1);
-            mbar_init(&B.k_empty[s], 1);
             mbar_init(&B.v_full[s], 1);
             mbar_init(&B.v_empty[s], 1);
             mbar_init(&B.s_full[s], 1);
             mbar_init(&B.s_free[s], 128);
+            mbar_init(&B.p_full[s], 128);
+            mbar_init(&B.pv_done[s], 1);
         }
-        mbar_init(B.p_full, 128);
-        mbar_init(B.pv_done, 1);
         mbar_init(B.drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -144,21 +153,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;
+    const uint32_t tmem = *tmem_slot;  // S_A at +0, S_B at +128, O_A at +256, O_B at +384
 
     if (warp == 0) {
         // ================================ TMA producer ================================
         const uint64_t pol_q = l2_evict_first_policy();
         const uint64_t pol_kv = l2_evict_normal_policy();
-        int issued = 0;  // KV tiles armed
+        int k_issued = 0, v_issued = 0;
         if (lane == 0) {
             tma_prefetch_map(&maps.q);
             tma_prefetch_map(&maps.k);
             tma_prefetch_map(&maps.v);
-            mbar_arrive_expect_tx(B.q_full, kTileBytes);
-            tma_load_3d(smem + kOffQ, &maps.q, 0, j, q0 + qt * kBM, B.q_full, pol_q);
-            tma_load_3d(smem + kOffQ + kPanel, &maps.q, 64, j, q0 + qt * kBM, B.q_full, pol_q);
+            mbar_arrive_expect_tx(B.q_full, 2 * kTileBytes);
+            for (int x = 0; x < 2; ++x) {
+                tma_load_3d(smem + kOffQ + x * kTileBytes, &maps.q, 0, j, row0 + x * kBM, B.q_full, pol_q);
+                tma_load_3d(smem + kOffQ + x * kTileBytes + kPanel, &maps.q, 64, j, row0 + x * kBM, B.q_full,
+                            pol_q);
+            }
         }
         const int32_t* trow = a.block_table + (int64_t)c * a.max_blocks;
         // lane g < 8 loads the block id of page g of tile t (keys 128t + 16g ..)
@@ -168,7 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int32_t blk_next = fetch(0);
         for (int t = 0; t < n_kv; ++t) {
-            const int stage = t & 1;
             const int32_t blk = blk_next;
             blk_next = fetch(t + 1);  // in flight while this tile is issued
             int y = 0;
@@ -184,45 +194,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const unsigned pages = __ballot_sync(0xffffffffu, have);
             const uint32_t bytes = (uint32_t)__popc(pages) * 2u * (kPage * 128u);
+            // K (one stage): free once S_A(t-1) and S_B(t-1) are done
             bool go = true;
             if (lane == 0) {
-                if (t >= 2) go = wait_or_abort(&B.k_empty[stage], ((t >> 1) - 1) & 1, abort_flag, a.status);
-                else go = !*abort_flag;
-                if (go) mbar_arrive_expect_tx(&B.k_full[stage], bytes);
+                go = t >= 1 ? wait_or_abort(B.k_empty, (t - 1) & 1, abort_flag, a.status) : !*abort_flag;
+                if (go) mbar_arrive_expect_tx(B.k_full, bytes);
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
             for (int g = 0; g < kBN / kPage; ++g) {
                 const int yg = __shfl_sync(0xffffffffu, y, g);
                 if (lane == 0 && ((pages >> g) & 1u)) {
-                    unsigned char* dst = smem + kOffK + stage * kTileBytes + g * (kPage * 128);
-                    tma_load_2d(dst, &maps.k, 0, yg, &B.k_full[stage], pol_kv);
-                    tma_load_2d(dst + kPanel, &maps.k, 64, yg, &B.k_full[stage], pol_kv);
+                    unsigned char* dst = smem + kOffK + g * (kPage * 128);
+                    tma_load_2d(dst, &maps.k, 0, yg, B.k_full, pol_kv);
+                    tma_load_2d(dst + kPanel, &maps.k, 64, yg, B.k_full, pol_kv);
                 }
             }
+            k_issued = t + 1;
+            // V (two stages): stage t&1 free once PV_A(t-2) and PV_B(t-2) are done
+            const int vs = t & 1;
             if (lane == 0) {
-                if (t >= 2) go = wait_or_abort(&B.v_empty[stage], ((t >> 1) - 1) & 1, abort_flag, a.status);
-                else go = !*abort_flag;
-                if (go) mbar_arrive_expect_tx(&B.v_full[stage], bytes);
+                go = t >= 2 ? wait_or_abort(&B.v_empty[vs], ((t >> 1) - 1) & 1, abort_flag, a.status)
+                            : !*abort_flag;
+                if (go) mbar_arrive_expect_tx(&B.v_full[vs], bytes);
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
             for (int g = 0; g < kBN / kPage; ++g) {
                 const int yg = __shfl_sync(0xffffffffu, y, g);
                 if (lane == 0 && ((pages >> g) & 1u)) {
-                    unsigned char* dst = smem + kOffV + stage * kTileBytes + g * (kPage * 128);
-                    tma_load_2d(dst, &maps.v, 0, yg, &B.v_full[stage], pol_kv);
-                    tma_load_2d(dst + kPanel, &maps.v, 64, yg, &B.v_full[stage], pol_kv);
+                    unsigned char* dst = smem + kOffV + vs * kTileBytes + g * (kPage * 128);
+                    tma_load_2d(dst, &maps.v, 0, yg, &B.v_full[vs], pol_kv);
+                    tma_load_2d(dst + kPanel, &maps.v, 64, yg, &B.v_full[vs], pol_kv);
                 }
             }
-            issued = t + 1;
+            v_issued = t + 1;
         }
         // After an abort, let every armed copy land before the CTA can exit.
         if (lane == 0 && *abort_flag) {
-            for (int t = max(0, issued - 2); t < issued; ++t) {
-                mbar_wait(&B.k_full[t & 1], (t >> 1) & 1, a.status);
-                mbar_wait(&B.v_full[t & 1], (t >> 1) & 1, a.status);
-            }
+            if (k_issued > 0) mbar_wait(B.k_full, (k_issued - 1) & 1, a.status);
+            for (int t = max(0, v_issued - 2); t < v_issued; ++t) mbar_wait(&B.v_full[t & 1], (t >> 1) & 1, a.status);
             mbar_wait(B.q_full, 0, a.status);
         }
     } else if (warp == 1) {
@@ -230,41 +241,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kHD, true);
-            const uint32_t sQ = smem_addr(smem + kOffQ), sP = smem_addr(smem + kOffP);
-            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status);
-            auto issue_s = [&](int t) -> bool {
-                const int stage = t & 1;
-                if (!wait_or_abort(&B.k_full[stage], (t >> 1) & 1, abort_flag, a.status)) return false;
-                if (t >= 2 && !wait_or_abort(&B.s_free[stage], ((t >> 1) - 1) & 1, abort_flag, a.status))
-                    return false;
-                tc_fence_after();
-                const uint32_t sK = smem_addr(smem + kOffK + stage * kTileBytes);
+            const uint32_t sK = smem_addr(smem + kOffK);
+            auto issue_s = [&](int x) {  // S_x = Q_x K^T
+                const uint32_t sQ = smem_addr(smem + kOffQ + x * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < kHD / 16; ++k) {
                     const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-                    tc_mma_f16(tmem + stage * 128, umma_desc_sw128(sQ + off, 16, 1024),
+                    tc_mma_f16(tmem + x * 128, umma_desc_sw128(sQ + off, 16, 1024),
                                umma_desc_sw128(sK + off, 16, 1024), idesc_s, k > 0);
                 }
-                tc_commit(&B.s_full[stage]);
-                tc_commit(&B.k_empty[stage]);
-                return true;
+                tc_commit(&B.s_full[x]);
             };
-            if (ok) ok = issue_s(0);
-            for (int t = 0; ok && t < n_kv; ++t) {
-                if (t + 1 < n_kv && !issue_s(t + 1)) break;
-                const int stage = t & 1;
-                if (!wait_or_abort(&B.v_full[stage], (t >> 1) & 1, abort_flag, a.status)) break;
-                if (!wait_or_abort(B.p_full, t & 1, abort_flag, a.status)) break;
-                tc_fence_after();
-                const uint32_t sV = smem_addr(smem + kOffV + stage * kTileBytes);
+            auto issue_pv = [&](int x, int t) {  // O_x += P_x V_t
+                const uint32_t sP = smem_addr(smem + kOffP + x * kTileBytes);
+                const uint32_t sV = smem_addr(smem + kOffV + (t & 1) * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k) {
                     const uint32_t offp = (k >> 2) * kPanel + (k & 3) * 32;
-                    tc_mma_f16(tO, umma_desc_sw128(sP + offp, 16, 1024),
+                    tc_mma_f16(tmem + 256 + x * 128, umma_desc_sw128(sP + offp, 16, 1024),
                                umma_desc_sw128(sV + k * 16 * 128, kPanel, 1024), idesc_o, (t > 0 || k > 0));
                 }
-                tc_commit(&B.v_empty[stage]);
-                tc_commit(B.pv_done);
+                tc_commit(&B.pv_done[x]);
+            };
+            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status) &&
+                      wait_or_abort(B.k_full, 0, abort_flag, a.status);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_s(1);
+                tc_commit(B.k_empty);
+            }
+            for (int t = 0; ok && t < n_kv; ++t) {
+                const bool more = t + 1 < n_kv;
+                // PV_A(t), then S_A(t+1)
+                if (!wait_or_abort(&B.v_full[t & 1], (t >> 1) & 1, abort_flag, a.status)) break;
+                if (!wait_or_abort(&B.p_full[0], t & 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                issue_pv(0, t);
+                if (more) {
+                    if (!wait_or_abort(B.k_full, (t + 1) & 1, abort_flag, a.status)) break;
+                    if (!wait_or_abort(&B.s_free[0], t & 1, abort_flag, a.status)) break;
+                    tc_fence_after();
+                    issue_s(0);
+                }
+                // PV_B(t), then S_B(t+1)
+                if (!wait_or_abort(&B.p_full[1], t & 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                issue_pv(1, t);
+                tc_commit(&B.v_empty[t & 1]);
+                if (more) {
+                    if (!wait_or_abort(&B.s_free[1], t & 1, abort_flag, a.status)) break;
+                    tc_fence_after();
+                    issue_s(1);
+                    tc_commit(B.k_empty);
+                }
             }
             // every MMA this thread issued has completed once `drain` flips
             tc_commit(B.drain);
@@ -272,34 +302,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ============================ softmax / epilogue ============================
+        const int x = (warp - 2) >> 2;            // tile A (0) or B (1)
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
-        const int r = quarter * 32 + lane;        // query row of this thread
+        const int r = quarter * 32 + lane;        // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const int pos_r = pos0 + r;
+        const uint32_t tS = tmem + x * 128, tO = tmem + 256 + x * 128;
+        const int pos_r = pos0 + x * kBM + r;     // absolute position of this row
+        const int pos_first = pos0 + x * kBM;     // ... of the tile's first row
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
-        unsigned char* sP = smem + kOffP;
+        unsigned char* sP = smem + kOffP + x * kTileBytes;
         for (int t = 0; t < n_kv; ++t) {
-            const int buf = t & 1;
-            if (!warp_wait(&B.s_full[buf], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            if (!warp_wait(&B.s_full[x], t & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
             uint32_t sv[kBN];
 #pragma unroll
             for (int i = 0; i < kBN / 32; ++i)
-                tmem_ld32(tmem + buf * 128 + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[i * 32]));
+                tmem_ld32(tS + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[i * 32]));
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&B.s_free[buf]);
+            mbar_arrive(&B.s_free[x]);
             // causal mask: keys past this row's position (only tiles that reach
-            // beyond the first row's position can have any)
-            const int lim = (t * kBN + kBN - 1 > pos0) ? pos_r - t * kBN : kBN - 1;  // last visible column
+            // beyond the tile's first row can have any)
+            const int lim = (t * kBN + kBN - 1 > pos_first) ? pos_r - t * kBN : kBN - 1;  // last visible column
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < kBN; ++i) {
-                const float x = i <= lim ? __uint_as_float(sv[i]) : -INFINITY;
-                sv[i] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                const float v = i <= lim ? __uint_as_float(sv[i]) : -INFINITY;
+                sv[i] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
             }
             const float m_tile = mx * sl2;
             float alpha = 1.f;
@@ -325,9 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rs0 += bf16lo(w);  // sum what the MMA will actually use
                 rs1 += bf16hi(w);
             }
-            const float rs = rs0 + rs1;
-            lsum = lsum * alpha + rs;
-            if (t > 0 && !warp_wait(B.pv_done, (t - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            lsum = lsum * alpha + (rs0 + rs1);
+            if (t > 0 && !warp_wait(&B.pv_done[x], (t - 1) & 1, abort_flag, a.status)) { ok = false; break; }
             // tcgen05.ld/st are warp-collective: the whole warp rescales if
             // any of its rows must (alpha is 1 for the others)
             if (__any_sync(0xffffffffu, rescale && t > 0)) {
@@ -344,11 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
             }
             // keys past the end of the sequence: V rows must be zero (stale
-            // cache slots may hold anything, and 0 * NaN is NaN)
-            if ((t + 1) * kBN > seq_len) {
-                if (!warp_wait(&B.v_full[buf], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            // cache slots may hold anything, and 0 * NaN is NaN).  Tile A's
+            // warps do it; PV_B(t) is issued after PV_A(t), after their signal.
+            if (x == 0 && (t + 1) * kBN > seq_len) {
+                if (!warp_wait(&B.v_full[t & 1], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
                 if (t * kBN + r >= seq_len) {
-                    unsigned char* vrow = smem + kOffV + buf * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+                    unsigned char* vrow = smem + kOffV + (t & 1) * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                     for (int pnl = 0; pnl < 2; ++pnl)
 #pragma unroll
@@ -368,20 +400,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(B.p_full);
+            mbar_arrive(&B.p_full[x]);
         }
         // epilogue: O / l -> bf16 rows of out
-        if (ok && warp_wait(B.pv_done, (n_kv - 1) & 1, abort_flag, a.status)) {
+        if (ok && warp_wait(&B.pv_done[x], (n_kv - 1) & 1, abort_flag, a.status)) {
             tc_fence_after();
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            __nv_bfloat16* orow =
-                reinterpret_cast<__nv_bfloat16*>(a.out) + ((int64_t)(q0 + qt * kBM + r) * a.hq + j) * kHD;
+            const int rr = x * kBM + r;  // row of the 256
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((int64_t)(row0 + rr) * a.hq + j) * kHD;
 #pragma unroll
             for (int i = 0; i < kHD / 32; ++i) {
                 uint32_t v[32];
                 tmem_ld32(tO + lane_base + i * 32, v);
                 tmem_ld_wait();
-                if (r < rows) {
+                if (rr < rows) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 w;
@@ -468,7 +500,7 @@ kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
         attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     if (attr_err != cudaSuccess) return KVATTN_ERR_CUDA;
-    const int n_qt = (a.max_q_len + kBM - 1) / kBM;
+    const int n_qt = (a.max_q_len + 2 * kBM - 1) / (2 * kBM);
     const int64_t grid = (int64_t)a.num_chunks * n_qt * a.hq;
     if (grid <= 0) return KVATTN_OK;
     if (grid > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
