@@ -151,29 +151,34 @@ __device__ __forceinline__ uint32_t bf16_bits(float x)
     return (uint32_t)(*reinterpret_cast<uint16_t*>(&h));
 }
 
-// Accurate rotation of one pair with the float-float twiddle.
-__device__ __forceinline__ void rotate_pair_ff(float x0, float x1, uint64_t u, const float4* sector, ff& y0,
-                                               ff& y1)
+// Rotation of one pair by the float-float twiddle (c, s): about 44 bits.
+__device__ __forceinline__ void rotate_pair_ff(float x0, float x1, const float4& cs, ff& y0, ff& y1)
 {
-    ff c, s;
-    accurate_twiddle(u, sector, c, s);
+    const ff c = {cs.x, cs.y}, s = {cs.z, cs.w};
     y0 = ff_add(ff_mul_f(c, x0), ff_neg(ff_mul_f(s, x1)));
     y1 = ff_add(ff_mul_f(s, x0), ff_mul_f(c, x1));
 }
 
-// Rotates the bf16 pair packed in `w` (low half = even element).
-__device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, float2 cs, uint64_t u, const float4* sector)
+// Rotates the bf16 pair packed in `w` (low half = even element) by the
+// float-float twiddle cs = (c_hi, c_lo, s_hi, s_lo).
+// Fast path: y = x0 c_hi - x1 s_hi + (x0 c_lo - x1 s_lo) in fp32; its error
+// is at most 3 * 2^-24 (|x0| + |x1|) (three roundings of terms bounded by
+// |x0| + |x1|; the twiddle itself is good to ~2^-44), so with
+// delta = 2^-21 (|x0| + |x1|), if y - delta and y + delta round to the same
+// bf16 value, that is the correctly rounded rotation.  Otherwise the pair is
+// recomputed in float-float and rounded from there.
+__device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const float4& cs)
 {
     const float x0 = bf16lo(w), x1 = bf16hi(w);
-    const float y0 = __fmaf_rn(x0, cs.x, -__fmul_rn(x1, cs.y));
-    const float y1 = __fmaf_rn(x0, cs.y, __fmul_rn(x1, cs.x));
-    const float delta = 0x1p-20f * (fabsf(x0) + fabsf(x1));
+    const float y0 = __fadd_rn(__fmaf_rn(x0, cs.x, -__fmul_rn(x1, cs.z)), __fmaf_rn(x0, cs.y, -__fmul_rn(x1, cs.w)));
+    const float y1 = __fadd_rn(__fmaf_rn(x0, cs.z, __fmul_rn(x1, cs.x)), __fmaf_rn(x0, cs.w, __fmul_rn(x1, cs.y)));
+    const float delta = 0x1p-21f * (fabsf(x0) + fabsf(x1));
     uint32_t b0 = bf16_bits(y0), b1 = bf16_bits(y1);
     const bool safe = bf16_bits(y0 - delta) == b0 && bf16_bits(y0 + delta) == b0 &&
                       bf16_bits(y1 - delta) == b1 && bf16_bits(y1 + delta) == b1;
     if (!safe) {
         ff z0, z1;
-        rotate_pair_ff(x0, x1, u, sector, z0, z1);
+        rotate_pair_ff(x0, x1, cs, z0, z1);
         b0 = rne_bf16_ff(z0);
         b1 = rne_bf16_ff(z1);
     }
@@ -186,11 +191,33 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
     constexpr int kPairs = kD / 2;
     constexpr int kEPV = kBF16 ? 8 : 4;  // elements per 16-byte vector
     constexpr int kVPH = kD / kEPV;      // vectors per head
-    __shared__ float2 tw[kPairs];
-    __shared__ uint64_t turns[kPairs];
+    constexpr int kBatch = 4;            // vectors a thread has in flight
+    constexpr int kE = kBF16 ? 2 : 4;
+    __shared__ float4 tw[kPairs];        // float-float (cos, sin) of every pair at this position
     __shared__ float4 sector[5];
 
-    const int t = blockIdx.x;
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int nq = a.hq * kVPH, nk = a.hkv * kVPH;
+    const int total = nq + 2 * nk;
+
+    // source and destination of vector v of this token (destination known once
+    // the block is)
+    auto src_of = [&](int v) -> const char* {
+        if (v < nq) return (const char*)a.q + ((int64_t)t * nq + v) * 16;
+        v -= nq;
+        const char* base = (const char*)(v < nk ? a.k : a.v);
+        if (v >= nk) v -= nk;
+        return base + ((int64_t)t * nk + v) * 16;
+    };
+
+    // first batch of loads: independent of the position lookups below
+    uint4 w[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+        const int v = tid + i * 128;
+        if (v < total) w[i] = *reinterpret_cast<const uint4*>(src_of(v));
+    }
+
     const int pos = a.positions[t];
     const int seq = a.seq_ids[t];
     bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
@@ -200,62 +227,65 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
         ok = blk >= 0 && blk < a.num_blocks;
     }
     if (!ok) {
-        if (threadIdx.x == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
+        if (tid == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
         return;
     }
     const int off = pos % a.block_size;
-
-    for (int i = threadIdx.x; i < kPairs; i += blockDim.x) {
-        const uint64_t u = (uint64_t)(uint32_t)pos * a.turns[i];
-        turns[i] = u;
-        float sn, cs;
-        // fraction of a turn in [-1/2, 1/2) -> half-turns for sincospif
-        sincospif((float)(int64_t)u * 0x1p-63f, &sn, &cs);
-        tw[i] = make_float2(cs, sn);
+    if (tid < 5) sector[tid] = a.sector[tid];
+    __syncthreads();
+    for (int i = tid; i < kPairs; i += 128) {
+        ff c, sn;
+        accurate_twiddle((uint64_t)(uint32_t)pos * a.turns[i], sector, c, sn);
+        tw[i] = make_float4(c.hi, c.lo, sn.hi, sn.lo);
     }
-    if (threadIdx.x < 5) sector[threadIdx.x] = a.sector[threadIdx.x];
     __syncthreads();
 
-    const int nq = a.hq * kVPH, nk = a.hkv * kVPH;
-    const int total = nq + 2 * nk;
-    for (int v = threadIdx.x; v < total; v += blockDim.x) {
-        int which, head, dv;
-        if (v < nq) {
-            which = 0; head = v / kVPH; dv = v - head * kVPH;
-        } else if (v < nq + nk) {
-            which = 1; head = (v - nq) / kVPH; dv = v - nq - head * kVPH;
-        } else {
-            which = 2; head = (v - nq - nk) / kVPH; dv = v - nq - nk - head * kVPH;
-        }
-        const int64_t eoff = (int64_t)dv * kEPV;
-        const char* src;
-        char* dst;
-        if (which == 0) {
-            src = (const char*)a.q + (((int64_t)t * a.hq + head) * kD + eoff) * (kBF16 ? 2 : 4);
-            dst = (char*)src;
-        } else {
-            const void* base = which == 1 ? a.k : a.v;
-            src = (const char*)base + (((int64_t)t * a.hkv + head) * kD + eoff) * (kBF16 ? 2 : 4);
-            void* pool = which == 1 ? a.k_pool : a.v_pool;
-            dst = (char*)pool + (((blk * a.hkv + head) * a.block_size + off) * kD + eoff) * (kBF16 ? 2 : 4);
-        }
-        uint4 w = *reinterpret_cast<const uint4*>(src);
-        if (which != 2) {
-            const int p0 = dv * (kEPV / 2);
-            if constexpr (kBF16) {
-                w.x = rotate_bf16_word(w.x, tw[p0 + 0], turns[p0 + 0], sector);
-                w.y = rotate_bf16_word(w.y, tw[p0 + 1], turns[p0 + 1], sector);
-                w.z = rotate_bf16_word(w.z, tw[p0 + 2], turns[p0 + 2], sector);
-                w.w = rotate_bf16_word(w.w, tw[p0 + 3], turns[p0 + 3], sector);
-            } else {
-                ff z0, z1, z2, z3;
-                rotate_pair_ff(__uint_as_float(w.x), __uint_as_float(w.y), turns[p0], sector, z0, z1);
-                rotate_pair_ff(__uint_as_float(w.z), __uint_as_float(w.w), turns[p0 + 1], sector, z2, z3);
-                w = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
-                               __float_as_uint(z3.hi));
+    for (int base = 0; base < total; base += kBatch * 128) {
+        if (base > 0) {
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int v = base + tid + i * 128;
+                if (v < total) w[i] = *reinterpret_cast<const uint4*>(src_of(v));
             }
         }
-        *reinterpret_cast<uint4*>(dst) = w;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int v = base + tid + i * 128;
+            if (v >= total) continue;
+            char* dst;
+            int dv;
+            bool rot = true;
+            if (v < nq) {
+                dst = (char*)a.q + ((int64_t)t * nq + v) * 16;
+                dv = v % kVPH;
+            } else {
+                int u = v - nq;
+                const bool isv = u >= nk;
+                if (isv) u -= nk;
+                rot = !isv;
+                const int head = u / kVPH;
+                dv = u - head * kVPH;
+                void* pool = isv ? a.v_pool : a.k_pool;
+                dst = (char*)pool + (((blk * a.hkv + head) * a.block_size + off) * kD + (int64_t)dv * kEPV) * kE;
+            }
+            uint4 x = w[i];
+            if (rot) {
+                const int p0 = dv * (kEPV / 2);
+                if constexpr (kBF16) {
+                    x.x = rotate_bf16_word(x.x, tw[p0 + 0]);
+                    x.y = rotate_bf16_word(x.y, tw[p0 + 1]);
+                    x.z = rotate_bf16_word(x.z, tw[p0 + 2]);
+                    x.w = rotate_bf16_word(x.w, tw[p0 + 3]);
+                } else {
+                    ff z0, z1, z2, z3;
+                    rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), tw[p0], z0, z1);
+                    rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), tw[p0 + 1], z2, z3);
+                    x = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
+                                   __float_as_uint(z3.hi));
+                }
+            }
+            *reinterpret_cast<uint4*>(dst) = x;
+        }
     }
 }
 
