@@ -159,30 +159,85 @@ __device__ __forceinline__ void rotate_pair_ff(float x0, float x1, const float4&
     y1 = ff_add(ff_mul_f(s, x0), ff_mul_f(c, x1));
 }
 
-// Rotates the bf16 pair packed in `w` (low half = even element) by the
-// float-float twiddle cs = (c_hi, c_lo, s_hi, s_lo).
-// Fast path: y = x0 c_hi - x1 s_hi + (x0 c_lo - x1 s_lo) in fp32; its error
-// is at most 3 * 2^-24 (|x0| + |x1|) (three roundings of terms bounded by
-// |x0| + |x1|; the twiddle itself is good to ~2^-44), so with
-// delta = 2^-21 (|x0| + |x1|), if y - delta and y + delta round to the same
-// bf16 value, that is the correctly rounded rotation.  Otherwise the pair is
-// recomputed in float-float and rounded from there.
-__device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const float4& cs)
+__device__ __forceinline__ uint64_t pk2(float lo, float hi)
+{
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// A pair's twiddle as packed operands: y = x0 * (c, s) + x1 * (-s, c), for the
+// high and the low float of the float-float (c, s).
+struct Twiddle2 {
+    uint64_t cs_hi, sc_hi, cs_lo, sc_lo;  // (c, s), (-s, c) for hi and lo
+    float4 ff;                            // (c_hi, c_lo, s_hi, s_lo) for the slow path
+};
+
+__device__ __forceinline__ Twiddle2 make_twiddle2(const float4& t)
+{
+    Twiddle2 w;
+    w.cs_hi = pk2(t.x, t.z);
+    w.sc_hi = pk2(-t.z, t.x);
+    w.cs_lo = pk2(t.y, t.w);
+    w.sc_lo = pk2(-t.w, t.y);
+    w.ff = t;
+    return w;
+}
+
+// Slow path of rotate_bf16_word, kept out of line: it runs for well under one
+// percent of the pairs and would otherwise bloat every inlined copy.
+__device__ __noinline__ uint32_t rotate_bf16_word_slow(float x0, float x1, float4 ff_cs)
+{
+    ff z0, z1;
+    rotate_pair_ff(x0, x1, ff_cs, z0, z1);
+    return rne_bf16_ff(z0) | (rne_bf16_ff(z1) << 16);
+}
+
+// RNE to bf16 of y is also the RNE of every value within delta of y when the
+// fp32 pattern of y is more than delta away from a bf16 rounding boundary
+// (low 16 bits 0x8000).  Distance in fp32 ulps times |y| over-estimates the
+// distance times 2^23 by at most 2x, hence the conservative test
+// dist * |y| > 2^24 * delta.  Near-zero results fail it and take the slow path.
+__device__ __forceinline__ bool rounding_safe(float y, float delta_x_2p24)
+{
+    const int r = (int)(__float_as_uint(y) & 0xffffu) - 0x8000;
+    return fabsf((float)r) * fabsf(y) > delta_x_2p24;
+}
+
+// Rotates the bf16 pair packed in `w` (low half = even element).
+// Fast path: y = x0 (c, s)_hi + x1 (-s, c)_hi + [x0 (c, s)_lo + x1 (-s, c)_lo]
+// in fp32; its error is at most 3 * 2^-24 (|x0| + |x1|) (three roundings of
+// terms bounded by |x0| + |x1|; the twiddle itself is good to ~2^-44), so with
+// delta = 2^-21 (|x0| + |x1|) a pattern that passes rounding_safe rounds to the
+// correctly rounded rotation.  Otherwise the pair is recomputed in
+// float-float and rounded from there.
+__device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const Twiddle2& tw)
 {
     const float x0 = bf16lo(w), x1 = bf16hi(w);
-    const float y0 = __fadd_rn(__fmaf_rn(x0, cs.x, -__fmul_rn(x1, cs.z)), __fmaf_rn(x0, cs.y, -__fmul_rn(x1, cs.w)));
-    const float y1 = __fadd_rn(__fmaf_rn(x0, cs.z, __fmul_rn(x1, cs.x)), __fmaf_rn(x0, cs.w, __fmul_rn(x1, cs.y)));
-    const float delta = 0x1p-21f * (fabsf(x0) + fabsf(x1));
-    uint32_t b0 = bf16_bits(y0), b1 = bf16_bits(y1);
-    const bool safe = bf16_bits(y0 - delta) == b0 && bf16_bits(y0 + delta) == b0 &&
-                      bf16_bits(y1 - delta) == b1 && bf16_bits(y1 + delta) == b1;
-    if (!safe) {
-        ff z0, z1;
-        rotate_pair_ff(x0, x1, cs, z0, z1);
-        b0 = rne_bf16_ff(z0);
-        b1 = rne_bf16_ff(z1);
-    }
-    return b0 | (b1 << 16);
+    const uint64_t xx0 = pk2(x0, x0), xx1 = pk2(x1, x1);
+    const uint64_t hi = ffma2(xx1, tw.sc_hi, fmul2(xx0, tw.cs_hi));
+    const uint64_t lo = ffma2(xx1, tw.sc_lo, fmul2(xx0, tw.cs_lo));
+    const uint64_t y = fadd2(hi, lo);
+    const float y0 = __uint_as_float((uint32_t)y), y1 = __uint_as_float((uint32_t)(y >> 32));
+    const float dx = 8.0f * (fabsf(x0) + fabsf(x1));  // 2^24 * 2^-21 * (|x0| + |x1|)
+    if (rounding_safe(y0, dx) && rounding_safe(y1, dx)) return pack_bf16_rn(y0, y1);
+    return rotate_bf16_word_slow(x0, x1, tw.ff);
 }
 
 template <bool kBF16, int kD>
@@ -191,32 +246,32 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
     constexpr int kPairs = kD / 2;
     constexpr int kEPV = kBF16 ? 8 : 4;  // elements per 16-byte vector
     constexpr int kVPH = kD / kEPV;      // vectors per head
-    constexpr int kBatch = 4;            // vectors a thread has in flight
+    constexpr int kPPV = kEPV / 2;       // pairs per vector
+    constexpr int kGroups = 128 / kVPH;  // threads sharing one column slice
     constexpr int kE = kBF16 ? 2 : 4;
+    constexpr int kMaxV = 8;             // vectors a thread keeps in flight
     __shared__ float4 tw[kPairs];        // float-float (cos, sin) of every pair at this position
     __shared__ float4 sector[5];
 
     const int t = blockIdx.x, tid = threadIdx.x;
-    const int nq = a.hq * kVPH, nk = a.hkv * kVPH;
-    const int total = nq + 2 * nk;
-
-    // source and destination of vector v of this token (destination known once
-    // the block is)
-    auto src_of = [&](int v) -> const char* {
-        if (v < nq) return (const char*)a.q + ((int64_t)t * nq + v) * 16;
-        v -= nq;
-        const char* base = (const char*)(v < nk ? a.k : a.v);
-        if (v >= nk) v -= nk;
-        return base + ((int64_t)t * nk + v) * 16;
+    // this thread: column slice dv (fixed), heads hg, hg + kGroups, ... of q, k, v
+    const int dv = tid % kVPH, hg = tid / kVPH;
+    const int nq = (a.hq - hg + kGroups - 1) / kGroups;   // q heads of this thread
+    const int nk = (a.hkv - hg + kGroups - 1) / kGroups;  // k (and v) heads of this thread
+    const int nv = max(0, nq) + 2 * max(0, nk);
+    auto src_of = [&](int i) -> const char* {  // i-th vector of this thread
+        if (i < nq) return (const char*)a.q + (((int64_t)t * a.hq + hg + i * kGroups) * kD + dv * kEPV) * kE;
+        i -= nq;
+        const char* base = (const char*)(i < nk ? a.k : a.v);
+        if (i >= nk) i -= nk;
+        return base + (((int64_t)t * a.hkv + hg + i * kGroups) * kD + dv * kEPV) * kE;
     };
 
-    // first batch of loads: independent of the position lookups below
-    uint4 w[kBatch];
+    // first loads: independent of the position lookups below
+    uint4 w[kMaxV];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-        const int v = tid + i * 128;
-        if (v < total) w[i] = *reinterpret_cast<const uint4*>(src_of(v));
-    }
+    for (int i = 0; i < kMaxV; ++i)
+        if (i < nv) w[i] = *reinterpret_cast<const uint4*>(src_of(i));
 
     const int pos = a.positions[t];
     const int seq = a.seq_ids[t];
@@ -239,47 +294,44 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
         tw[i] = make_float4(c.hi, c.lo, sn.hi, sn.lo);
     }
     __syncthreads();
+    Twiddle2 tws[kPPV];
+#pragma unroll
+    for (int p = 0; p < kPPV; ++p) tws[p] = make_twiddle2(tw[dv * kPPV + p]);
 
-    for (int base = 0; base < total; base += kBatch * 128) {
+    for (int base = 0; base < nv; base += kMaxV) {
         if (base > 0) {
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int v = base + tid + i * 128;
-                if (v < total) w[i] = *reinterpret_cast<const uint4*>(src_of(v));
-            }
+            for (int i = 0; i < kMaxV; ++i)
+                if (base + i < nv) w[i] = *reinterpret_cast<const uint4*>(src_of(base + i));
         }
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int v = base + tid + i * 128;
-            if (v >= total) continue;
+        for (int ii = 0; ii < kMaxV; ++ii) {
+            const int i = base + ii;
+            if (i >= nv) break;
             char* dst;
-            int dv;
             bool rot = true;
-            if (v < nq) {
-                dst = (char*)a.q + ((int64_t)t * nq + v) * 16;
-                dv = v % kVPH;
+            if (i < nq) {
+                dst = const_cast<char*>(src_of(i));
             } else {
-                int u = v - nq;
+                int u = i - nq;
                 const bool isv = u >= nk;
                 if (isv) u -= nk;
                 rot = !isv;
-                const int head = u / kVPH;
-                dv = u - head * kVPH;
                 void* pool = isv ? a.v_pool : a.k_pool;
+                const int64_t head = hg + u * kGroups;
                 dst = (char*)pool + (((blk * a.hkv + head) * a.block_size + off) * kD + (int64_t)dv * kEPV) * kE;
             }
-            uint4 x = w[i];
+            uint4 x = w[ii];
             if (rot) {
-                const int p0 = dv * (kEPV / 2);
                 if constexpr (kBF16) {
-                    x.x = rotate_bf16_word(x.x, tw[p0 + 0]);
-                    x.y = rotate_bf16_word(x.y, tw[p0 + 1]);
-                    x.z = rotate_bf16_word(x.z, tw[p0 + 2]);
-                    x.w = rotate_bf16_word(x.w, tw[p0 + 3]);
+                    x.x = rotate_bf16_word(x.x, tws[0]);
+                    x.y = rotate_bf16_word(x.y, tws[1]);
+                    x.z = rotate_bf16_word(x.z, tws[2]);
+                    x.w = rotate_bf16_word(x.w, tws[3]);
                 } else {
                     ff z0, z1, z2, z3;
-                    rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), tw[p0], z0, z1);
-                    rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), tw[p0 + 1], z2, z3);
+                    rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), tws[0].ff, z0, z1);
+                    rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), tws[1].ff, z2, z3);
                     x = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
                                    __float_as_uint(z3.hi));
                 }
