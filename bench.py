@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 METRIC = "decode attention KV-read GB/s and % of GB300 HBM peak; query tokens/s"
-DEFAULT_WORKLOAD = "c4"
+DEFAULT_WORKLOAD = "c5"   # the only workload whose step runs every stage: allocator, rope_append, prefill, decode
 
 
 def parse_args():
@@ -63,6 +63,30 @@ def peaks():
         return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1898.0)), float(
             d.get("bf16_tflops_sustained", 1718.7)), "measured"
     return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- ncu traffic
+
+KERNEL_SOURCES = {"decode_split+decode_combine": "decode.cu", "prefill_chunk": "prefill.cu",
+                  "rope_append": "rope_append.cu"}
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from the
+    committed ncu summary, or None when it was taken on other source code."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = KERNEL_SOURCES.get(kernel)
+    if not src or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel, {}).get(workload)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, "kv_cache_attention_rope_gb300", "csrc", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return rec["bytes_per_launch"] if rec.get("source_sha256") == sha else None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -241,6 +265,7 @@ class Step:
         nws = kv.decode_workspace_size(self.cfg, max(1, self.n_dec), self.max_len, 0)
         self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=device)
         self.h_out = torch.empty(self.out_dec.shape, dtype=dt).pin_memory()
+        self.h_out_pre = torch.empty(self.out_pre.shape, dtype=dt).pin_memory()
         # algorithmic bytes / flops
         E = wl.elem_bytes
         self.kv_bytes_decode = workloads.kv_bytes_read(wl, total[nchunk:])
@@ -302,6 +327,8 @@ class Step:
             kv.decode(self.cfg, self.cache, self.q_dec, self.d_table_dec, self.lens, self.max_len, out=self.out_dec,
                       workspace=self.ws)
             self.h_out.copy_(self.out_dec, non_blocking=True)
+        if self.nchunk:
+            self.h_out_pre.copy_(self.out_pre, non_blocking=True)
         self.alloc_end(ids)
 
     def h2d_bytes(self) -> int:
@@ -310,7 +337,8 @@ class Step:
         return int(sum(t.numel() * t.element_size() for t in ts))
 
     def d2h_bytes(self) -> int:
-        return int(self.h_out.numel() * self.h_out.element_size()) if self.n_dec else 0
+        n = int(self.h_out.numel() * self.h_out.element_size()) if self.n_dec else 0
+        return n + (int(self.h_out_pre.numel() * self.h_out_pre.element_size()) if self.nchunk else 0)
 
 
 def oracle_sample(wl: workloads.Workload, target_s: float = 12.0, max_rows: int = 8):
@@ -428,20 +456,24 @@ def run_ours(args, rank, world):
     if not args.no_e2e:
         e2e = {"value": world * K * step_bytes / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": st.h2d_bytes(),
                "d2h_bytes_per_step": st.d2h_bytes(), "ms_per_step": 1e3 * e2e_t / K}
-    # dominant kernel roofline
+    # dominant kernel roofline (and the decode kernel's, the HBM-bound part)
     parts = {"decode": t_dec, "prefill": t_pre, "rope_append": t_rope}
     dom = max(parts, key=parts.get)
-    if dom == "prefill":
-        ach = st.prefill_flops / t_pre / 1e12
-        roof = {"kernel": "prefill_chunk", "bound": "tensor", "achieved": ach, "peak": bf16_sus, "unit": "TFLOP/s",
-                "frac": ach / bf16_sus, "traffic": None, "peak_source": f"bf16_tflops_sustained ({peak_src})"}
-    else:
-        k = "decode" if dom == "decode" else "rope_append"
+
+    def roof_of(k):
+        if k == "prefill":
+            ach = st.prefill_flops / t_pre / 1e12
+            return {"kernel": "prefill_chunk", "bound": "tensor", "achieved": ach, "peak": bf16_sus,
+                    "unit": "TFLOP/s", "frac": ach / bf16_sus,
+                    "traffic": measured_traffic("prefill_chunk", wl.key),
+                    "peak_source": f"bf16_tflops_sustained, {peak_src}"}
+        name = "decode_split+decode_combine" if k == "decode" else "rope_append"
         by = st.kv_bytes_decode if k == "decode" else st.rope_bytes
-        ach = by / parts[dom] / 1e9
-        roof = {"kernel": "decode_split+decode_combine" if k == "decode" else "rope_append", "bound": "hbm",
-                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
-                "peak_source": f"hbm_gbs ({peak_src})"}
+        ach = by / parts[k] / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": measured_traffic(name, wl.key), "peak_source": f"hbm_gbs, {peak_src}"}
+
+    roof = roof_of(dom)
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -459,6 +491,7 @@ def run_ours(args, rank, world):
         "kernels_ms": {k: 1e3 * v for k, v in parts.items()},
         "decode_kv_gbs": st.kv_bytes_decode / t_dec / 1e9 if st.n_dec else None,
         "roofline": roof,
+        "roofline_decode": roof_of("decode") if st.n_dec and dom != "decode" else None,
         "e2e": e2e,
         "gpu_launches": K * st.launches_per_step,
         "clocks": ck,
