@@ -65,6 +65,27 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# ----------------------------------------------------------------------------- multi-rank
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank floats over the process group (identity
+    when torch.distributed is not initialised): the job takes as long as its
+    slowest rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_elapsed_s: float) -> float:
+    """Units all ranks processed per second (weak scaling: every rank runs a replica)."""
+    return world * steps * units_per_rank_step / max_elapsed_s
+
+
 # ----------------------------------------------------------------------------- ncu traffic
 
 KERNEL_SOURCES = {"decode_split+decode_combine": "decode.cu", "prefill_chunk": "prefill.cu",
@@ -447,14 +468,12 @@ def run_ours(args, rank, world):
         e2.record(stream)
         torch.cuda.synchronize()
         e2e_t = s2.elapsed_time(e2) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed, e2e_t], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed, e2e_t = float(t[0]), float(t[1])
+    elapsed, e2e_t = max_over_ranks([elapsed, e2e_t], dev)
     step_bytes = st.kv_bytes_decode + st.kv_bytes_prefill
-    value = world * K * step_bytes / elapsed / 1e9
+    value = whole_job_rate(step_bytes, K, world, elapsed) / 1e9
     if not args.no_e2e:
-        e2e = {"value": world * K * step_bytes / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": st.h2d_bytes(),
+        e2e = {"value": whole_job_rate(step_bytes, K, world, e2e_t) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": st.h2d_bytes(),
                "d2h_bytes_per_step": st.d2h_bytes(), "ms_per_step": 1e3 * e2e_t / K}
     # dominant kernel roofline (and the decode kernel's, the HBM-bound part)
     parts = {"decode": t_dec, "prefill": t_pre, "rope_append": t_rope}
@@ -486,7 +505,7 @@ def run_ours(args, rank, world):
                    "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of KV per step)"
                    if step_bytes > 2e8 else "L2-resident: KV smaller than L2, not flushed",
                    "parallelism": f"replicas x{world}"},
-        "query_tokens_per_s": world * K * st.n_tok / elapsed,
+        "query_tokens_per_s": whole_job_rate(st.n_tok, K, world, elapsed),
         "hbm_frac": (st.kv_bytes_decode / t_dec / 1e9) / hbm if st.n_dec else None,
         "kernels_ms": {k: 1e3 * v for k, v in parts.items()},
         "decode_kv_gbs": st.kv_bytes_decode / t_dec / 1e9 if st.n_dec else None,

@@ -231,6 +231,16 @@ kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache*
 kvattn_status kvattn_get_device_status(void* stream, int32_t* out);
 
 /*
+ * kvattn_selftest_wait_timeout -- failure-detection self test, no counterpart
+ * on the pages.  Launches one CTA that waits on an mbarrier nothing will ever
+ * complete, through the same bounded wait every kvattn kernel uses, with a
+ * limit of limit_us microseconds (1 .. 1000000).  The wait runs out, the
+ * kernel records KVATTN_ERR_TIMEOUT in the device status word and returns; the
+ * context stays usable.  INVALID_ARG for a limit out of range.
+ */
+kvattn_status kvattn_selftest_wait_timeout(int32_t limit_us, void* stream);
+
+/*
  * Host-side block allocator (the CPU "block manager" of [Nano-vLLM],
  * section 05, and the page allocation of [RoPE page], section 5): a free
  * list of fixed-size block ids 0 .. num_blocks-1 in host memory, with a

@@ -33,7 +33,8 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTED = [
     "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_decode_workspace_size",
-    "kvattn_decode_num_splits", "kvattn_decode", "kvattn_decode_static_scratch", "kvattn_prefill_chunk", "kvattn_get_device_status",
+    "kvattn_decode_num_splits", "kvattn_decode", "kvattn_decode_static_scratch", "kvattn_prefill_chunk",
+    "kvattn_selftest_wait_timeout", "kvattn_get_device_status",
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
     "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
     "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
@@ -75,6 +76,7 @@ def _load():
         "kvattn_decode_static_scratch": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p], ctypes.c_int),
         "kvattn_prefill_chunk": ([cfgp, cachep, p, p, p, p, i32, i32, i32, i32, p, p], ctypes.c_int),
         "kvattn_get_device_status": ([p, ctypes.POINTER(i32)], ctypes.c_int),
+        "kvattn_selftest_wait_timeout": ([i32, p], ctypes.c_int),
         "kvattn_allocator_create": ([i64, ctypes.POINTER(p)], ctypes.c_int),
         "kvattn_allocator_destroy": ([p], None),
         "kvattn_alloc_blocks": ([p, i32, p], ctypes.c_int),
@@ -232,6 +234,11 @@ def get_device_status(stream=None) -> int:
     v = ctypes.c_int32(0)
     check(lib.kvattn_get_device_status(_stream(stream), ctypes.byref(v)), "kvattn_get_device_status")
     return int(v.value)
+
+
+def selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
+    """Runs the bounded-wait self test (records KVATTN_ERR_TIMEOUT on the device)."""
+    check(lib.kvattn_selftest_wait_timeout(int(limit_us), _stream(stream)), "kvattn_selftest_wait_timeout")
 
 
 def default_scale(head_dim: int) -> float:

@@ -120,6 +120,20 @@ void rope_tables(double base, int d, RopeArgs& a)
     }
 }
 
+// One CTA waits on an mbarrier that nothing will complete, through the same
+// bounded wait every kernel uses; the wait runs out and records
+// KVATTN_ERR_TIMEOUT.
+__global__ void selftest_timeout_kernel(int* status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait(&bar, 0, status, limit_ns);
+}
+
 }  // namespace
 }  // namespace kvattn
 
@@ -303,6 +317,15 @@ kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache*
     a.status = device_status_ptr();
     if (!a.status) return KVATTN_ERR_CUDA;
     return launch_prefill(a, static_cast<cudaStream_t>(stream));
+}
+
+kvattn_status kvattn_selftest_wait_timeout(int32_t limit_us, void* stream)
+{
+    if (limit_us < 1 || limit_us > 1000000) return KVATTN_ERR_INVALID_ARG;
+    int* st = device_status_ptr();
+    if (!st) return KVATTN_ERR_CUDA;
+    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st, (uint64_t)limit_us * 1000ull);
+    return cuda_status(cudaGetLastError());
 }
 
 kvattn_status kvattn_get_device_status(void* stream, int32_t* out)

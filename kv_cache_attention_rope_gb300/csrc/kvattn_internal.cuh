@@ -165,14 +165,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Bounded phase wait.  Returns false (and records KVATTN_ERR_TIMEOUT) if the
-// phase with the given parity has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status)
+// phase with the given parity has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             record_error(status, KVATTN_ERR_TIMEOUT);
             return false;
         }

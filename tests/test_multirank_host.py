@@ -1,0 +1,50 @@
+"""bench.py's multi-rank host logic with two gloo ranks on CPU: the job time is
+the slowest rank's, and the rate counts every rank's replica."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+
+        got = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.5])
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == [2.0, 10.0, 0.5]
+
+
+def test_single_process_identity_and_rate():
+    import bench
+
+    assert bench.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
+    # 2 ranks x 10 steps x 1e9 bytes in 4 s -> 5e9 bytes/s
+    assert bench.whole_job_rate(1e9, 10, 2, 4.0) == pytest.approx(5e9)
