@@ -17,9 +17,9 @@
 //  - warp 1 (one lane) issues the MMAs: S_x = Q_x K^T (M = N = 128, K = 128)
 //    and O_x += P_x V (V as an MN-major operand), x = A, B, all four
 //    accumulators in TMEM (512 columns); completion is signalled with
-//    tcgen05.commit on mbarriers.  The order S_A S_B | PV_A S_A' PV_B S_B' |
-//    ... keeps the tensor core busy with one tile while the other's softmax
-//    runs (ping-pong).
+//    tcgen05.commit on mbarriers.  The order S_A(j) S_B(j) PV_A(j-1)
+//    PV_B(j-1) keeps the tensor core busy with the next S pair while the
+//    softmax of the previous tile runs (ping-pong).
 //  - warps 2-5 (tile A) and 6-9 (tile B) own one query row per thread
 //    (= TMEM lane): load the row of S
 //    from TMEM, apply the causal mask on diagonal tiles, keep the running max
@@ -98,9 +98,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // One CTA: query rows [256 qt, 256 qt + 256) of chunk c, head j, as tiles A
-// (first 128 rows) and B (next 128), both against the same K/V stream.  The
-// MMA order S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ... keeps the
-// tensor core on one tile while the other tile's softmax runs.
+// (first 128 rows) and B (next 128), both against the same K/V stream.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ Maps maps, const int n_qt)
 {
@@ -263,39 +261,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&B.pv_done[x]);
             };
-            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status) &&
-                      wait_or_abort(B.k_full, 0, abort_flag, a.status);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-                issue_s(1);
-                tc_commit(B.k_empty);
-            }
-            for (int t = 0; ok && t < n_kv; ++t) {
-                const bool more = t + 1 < n_kv;
-                // PV_A(t), then S_A(t+1)
-                if (!wait_or_abort(&B.v_full[t & 1], (t >> 1) & 1, abort_flag, a.status)) break;
-                if (!wait_or_abort(&B.p_full[0], t & 1, abort_flag, a.status)) break;
+            // Order S_A(j) S_B(j) PV_A(j-1) PV_B(j-1): a tile's softmax has the
+            // whole next S pair to finish before its P.V is needed.  S_x(j)
+            // reuses S_x's TMEM columns once the softmax has read S_x(j-1)
+            // (s_free); P lives in shared memory.
+            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status);
+            auto do_pv = [&](int t) -> bool {  // PV_A(t), PV_B(t)
+                if (!wait_or_abort(&B.v_full[t & 1], (t >> 1) & 1, abort_flag, a.status)) return false;
+                if (!wait_or_abort(&B.p_full[0], t & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
                 issue_pv(0, t);
-                if (more) {
-                    if (!wait_or_abort(B.k_full, (t + 1) & 1, abort_flag, a.status)) break;
-                    if (!wait_or_abort(&B.s_free[0], t & 1, abort_flag, a.status)) break;
-                    tc_fence_after();
-                    issue_s(0);
-                }
-                // PV_B(t), then S_B(t+1)
-                if (!wait_or_abort(&B.p_full[1], t & 1, abort_flag, a.status)) break;
+                if (!wait_or_abort(&B.p_full[1], t & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
                 issue_pv(1, t);
                 tc_commit(&B.v_empty[t & 1]);
-                if (more) {
-                    if (!wait_or_abort(&B.s_free[1], t & 1, abort_flag, a.status)) break;
-                    tc_fence_after();
-                    issue_s(1);
-                    tc_commit(B.k_empty);
-                }
+                return true;
+            };
+            for (int t = 0; ok && t < n_kv; ++t) {
+                if (!wait_or_abort(B.k_full, t & 1, abort_flag, a.status)) break;
+                if (t > 0 && !wait_or_abort(&B.s_free[0], (t - 1) & 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                issue_s(0);
+                if (t > 0 && !wait_or_abort(&B.s_free[1], (t - 1) & 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                issue_s(1);
+                tc_commit(B.k_empty);
+                if (t > 0 && !do_pv(t - 1)) { ok = false; break; }
             }
+            if (ok) do_pv(n_kv - 1);
             // every MMA this thread issued has completed once `drain` flips
             tc_commit(B.drain);
             mbar_wait(B.drain, 0, a.status);
