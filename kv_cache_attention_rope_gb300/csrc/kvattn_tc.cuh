@@ -62,6 +62,18 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+// D (TMEM, fp32) (+)= A (TMEM: row i in lane i, two bf16 per 32-bit column,
+// K-major) x B (smem descriptor); one thread.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrives (once) on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar)

@@ -11,21 +11,29 @@
 // How (GB300 design), one CTA per (chunk, 256 query rows, query head), the
 // rows split into two 128-row tiles A and B that share one K/V stream:
 //  - warp 0 (one lane) streams with TMA tensor copies: both 128 x 128 bf16 Q
-//    tiles once, then 128-key K and V tiles, each gathered as eight 16-token
-//    pages of the KV head straight from the block table (K in one stage, V in
-//    two), 128-byte swizzled (the layout the MMA reads).
-//  - warp 1 (one lane) issues the MMAs: S_x = Q_x K^T (M = N = 128, K = 128)
-//    and O_x += P_x V (V as an MN-major operand), x = A, B, all four
-//    accumulators in TMEM (512 columns); completion is signalled with
-//    tcgen05.commit on mbarriers.  The order S_A(j) S_B(j) PV_A(j-1)
-//    PV_B(j-1) keeps the tensor core busy with the next S pair while the
-//    softmax of the previous tile runs (ping-pong).
+//    tiles once, then 128-key K and V tiles (two stages each), each gathered
+//    as eight 16-token pages of the KV head straight from the block table,
+//    128-byte swizzled (the layout the MMA reads).
+//  - warp 1 (one lane) issues the MMAs: S_x = Q_x K^T (M = N = 128, K = 128,
+//    both operands in shared memory) and O_x += P_x V (P_x read from TMEM,
+//    V an MN-major shared-memory operand), x = A, B.  TMEM (512 columns)
+//    holds S_A, S_B, O_A, O_B; P_x (bf16, 64 columns) overwrites the first
+//    half of S_x once the softmax has read it.  Taking P from TMEM halves the
+//    shared-memory operand traffic of P.V, which at N = 128 would otherwise
+//    saturate shared-memory bandwidth before the tensor core.
+//    Issue order per KV tile j: PV_A(j) S_A(j+1) PV_B(j) S_B(j+1): tensor
+//    operations of one thread run in issue order, so S_A(j+1) overwrites
+//    S_A's columns only after PV_A(j) has read P_A(j) from them, and while
+//    the softmax of tile A works on S_A(j+1) the tensor core runs PV_B(j) and
+//    S_B(j+1) (ping-pong).  Completion is signalled with tcgen05.commit on
+//    mbarriers; a commit covers every earlier MMA of the thread, so when
+//    S_x(j+1) is reported done, PV_x(j) is too and O_x may be rescaled.
 //  - warps 2-5 (tile A) and 6-9 (tile B) own one query row per thread
-//    (= TMEM lane): load the row of S
-//    from TMEM, apply the causal mask on diagonal tiles, keep the running max
-//    (raised only when it grows by more than 2^8, which bounds p by 256 and
-//    keeps the O rescale rare), write P as bf16 into shared memory for the
-//    next MMA, and finally read O, divide by the row sum and store bf16.
+//    (= TMEM lane): load the row of S from TMEM, apply the causal mask on
+//    diagonal tiles, keep the running max (raised only when it grows by more
+//    than 2^8, which bounds p by 256 and keeps the O rescale rare), write P
+//    as bf16 into TMEM for the next MMA, and finally read O, divide by the
+//    row sum and store bf16.
 //  - Every wait is bounded (1 s): a timeout records KVATTN_ERR_TIMEOUT, the
 //    roles stop waiting, drain their in-flight copies and MMAs, free TMEM and
 //    return.
@@ -42,15 +50,16 @@ constexpr int kBN = 128;      // keys per KV tile
 constexpr int kHD = 128;      // head dim
 constexpr int kPage = 16;     // tokens per TMA copy of one block
 constexpr int kThreads = 320; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, warps 6-9 softmax B
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
 
-constexpr int kTileBytes = kBM * kHD * 2;  // 32 KB: a Q tile, the K stage, a V stage or a P tile
+constexpr int kTileBytes = kBM * kHD * 2;  // 32 KB: a Q tile, a K stage or a V stage
 constexpr int kPanel = kTileBytes / 2;     // 16 KB: 128 rows x 64 columns
 constexpr int kOffQ = 0;                   // Q_A, Q_B
-constexpr int kOffK = 2 * kTileBytes;      // one stage
-constexpr int kOffV = 3 * kTileBytes;      // two stages
-constexpr int kOffP = 5 * kTileBytes;      // P_A, P_B
-constexpr int kOffBar = 7 * kTileBytes;
-constexpr int kNumBars = 16;
+constexpr int kOffK = 2 * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack to align the base to 1 KB
 
 struct Maps {
@@ -61,14 +70,13 @@ struct Maps {
 
 struct Bars {
     uint64_t* q_full;
-    uint64_t* k_full;
-    uint64_t* k_empty;
-    uint64_t* v_full;   // [2]
-    uint64_t* v_empty;  // [2]
+    uint64_t* k_full;   // [kKStages]
+    uint64_t* k_empty;  // [kKStages]
+    uint64_t* v_full;   // [kVStages]
+    uint64_t* v_empty;  // [kVStages]
     uint64_t* s_full;   // [2]: tile A, tile B
-    uint64_t* s_free;   // [2]
     uint64_t* p_full;   // [2]
-    uint64_t* pv_done;  // [2]
+    uint64_t* o_done;   // [2]: the last P.V of the tile has completed
     uint64_t* drain;
 };
 
@@ -89,6 +97,13 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Whole-warp wait: every lane waits, the warp agrees (tcgen05.ld/st that
 // follow are warp-collective, so a partial warp must never reach them).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status)
@@ -105,7 +120,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    Bars B{bar + 0, bar + 1, bar + 2, bar + 3, bar + 5, bar + 7, bar + 9, bar + 11, bar + 13, bar + 15};
+    Bars B;
+    {
+        uint64_t* b = bar;
+        B.q_full = b; b += 1;
+        B.k_full = b; b += kKStages;
+        B.k_empty = b; b += kKStages;
+        B.v_full = b; b += kVStages;
+        B.v_empty = b; b += kVStages;
+        B.s_full = b; b += 2;
+        B.p_full = b; b += 2;
+        B.o_done = b; b += 2;
+        B.drain = b;
+    }
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -133,15 +160,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 1);
-        mbar_init(B.k_full, 1);
-        mbar_init(B.k_empty, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&B.k_full[s], 1);
+            mbar_init(&B.k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(&B.v_full[s], 1);
             mbar_init(&B.v_empty[s], 1);
-            mbar_init(&B.s_full[s], 1);
-            mbar_init(&B.s_free[s], 128);
-            mbar_init(&B.p_full[s], 128);
-            mbar_init(&B.pv_done[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&B.s_full[x], 1);
+            mbar_init(&B.p_full[x], 128);
+            mbar_init(&B.o_done[x], 1);
         }
         mbar_init(B.drain, 1);
         *abort_flag = 0;
@@ -192,28 +222,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const unsigned pages = __ballot_sync(0xffffffffu, have);
             const uint32_t bytes = (uint32_t)__popc(pages) * 2u * (kPage * 128u);
-            // K (one stage): free once S_A(t-1) and S_B(t-1) are done
+            // K stage t % kKStages: free once S_A and S_B of tile t - kKStages are done
+            const int ks = t % kKStages;
             bool go = true;
             if (lane == 0) {
-                go = t >= 1 ? wait_or_abort(B.k_empty, (t - 1) & 1, abort_flag, a.status) : !*abort_flag;
-                if (go) mbar_arrive_expect_tx(B.k_full, bytes);
+                go = t >= kKStages ? wait_or_abort(&B.k_empty[ks], ((t / kKStages) - 1) & 1, abort_flag, a.status)
+                                   : !*abort_flag;
+                if (go) mbar_arrive_expect_tx(&B.k_full[ks], bytes);
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
             for (int g = 0; g < kBN / kPage; ++g) {
                 const int yg = __shfl_sync(0xffffffffu, y, g);
                 if (lane == 0 && ((pages >> g) & 1u)) {
-                    unsigned char* dst = smem + kOffK + g * (kPage * 128);
-                    tma_load_2d(dst, &maps.k, 0, yg, B.k_full, pol_kv);
-                    tma_load_2d(dst + kPanel, &maps.k, 64, yg, B.k_full, pol_kv);
+                    unsigned char* dst = smem + kOffK + ks * kTileBytes + g * (kPage * 128);
+                    tma_load_2d(dst, &maps.k, 0, yg, &B.k_full[ks], pol_kv);
+                    tma_load_2d(dst + kPanel, &maps.k, 64, yg, &B.k_full[ks], pol_kv);
                 }
             }
             k_issued = t + 1;
-            // V (two stages): stage t&1 free once PV_A(t-2) and PV_B(t-2) are done
-            const int vs = t & 1;
+            // V stage t % kVStages: free once PV_A and PV_B of tile t - kVStages are done
+            const int vs = t % kVStages;
             if (lane == 0) {
-                go = t >= 2 ? wait_or_abort(&B.v_empty[vs], ((t >> 1) - 1) & 1, abort_flag, a.status)
-                            : !*abort_flag;
+                go = t >= kVStages ? wait_or_abort(&B.v_empty[vs], ((t / kVStages) - 1) & 1, abort_flag, a.status)
+                                   : !*abort_flag;
                 if (go) mbar_arrive_expect_tx(&B.v_full[vs], bytes);
             }
             go = __shfl_sync(0xffffffffu, go, 0);
@@ -230,8 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // After an abort, let every armed copy land before the CTA can exit.
         if (lane == 0 && *abort_flag) {
-            if (k_issued > 0) mbar_wait(B.k_full, (k_issued - 1) & 1, a.status);
-            for (int t = max(0, v_issued - 2); t < v_issued; ++t) mbar_wait(&B.v_full[t & 1], (t >> 1) & 1, a.status);
+            for (int t = max(0, k_issued - kKStages); t < k_issued; ++t)
+                mbar_wait(&B.k_full[t % kKStages], (t / kKStages) & 1, a.status);
+            for (int t = max(0, v_issued - kVStages); t < v_issued; ++t)
+                mbar_wait(&B.v_full[t % kVStages], (t / kVStages) & 1, a.status);
             mbar_wait(B.q_full, 0, a.status);
         }
     } else if (warp == 1) {
@@ -239,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kHD, true);
-            const uint32_t sK = smem_addr(smem + kOffK);
-            auto issue_s = [&](int x) {  // S_x = Q_x K^T
+            auto issue_s = [&](int x, int t) {  // S_x = Q_x K_t^T
                 const uint32_t sQ = smem_addr(smem + kOffQ + x * kTileBytes);
+                const uint32_t sK = smem_addr(smem + kOffK + (t % kKStages) * kTileBytes);
 #pragma unroll
                 for (int k = 0; k < kHD / 16; ++k) {
                     const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
@@ -250,45 +284,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&B.s_full[x]);
             };
-            auto issue_pv = [&](int x, int t) {  // O_x += P_x V_t
-                const uint32_t sP = smem_addr(smem + kOffP + x * kTileBytes);
-                const uint32_t sV = smem_addr(smem + kOffV + (t & 1) * kTileBytes);
+            auto issue_pv = [&](int x, int t) {  // O_x += P_x V_t, P_x in S_x's first 64 columns
+                const uint32_t sV = smem_addr(smem + kOffV + (t % kVStages) * kTileBytes);
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k) {
-                    const uint32_t offp = (k >> 2) * kPanel + (k & 3) * 32;
-                    tc_mma_f16(tmem + 256 + x * 128, umma_desc_sw128(sP + offp, 16, 1024),
-                               umma_desc_sw128(sV + k * 16 * 128, kPanel, 1024), idesc_o, (t > 0 || k > 0));
-                }
-                tc_commit(&B.pv_done[x]);
+                for (int k = 0; k < kBN / 16; ++k)
+                    tc_mma_f16_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8,
+                                  umma_desc_sw128(sV + k * 16 * 128, kPanel, 1024), idesc_o, (t > 0 || k > 0));
             };
-            // Order S_A(j) S_B(j) PV_A(j-1) PV_B(j-1): a tile's softmax has the
-            // whole next S pair to finish before its P.V is needed.  S_x(j)
-            // reuses S_x's TMEM columns once the softmax has read S_x(j-1)
-            // (s_free); P lives in shared memory.
-            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status);
-            auto do_pv = [&](int t) -> bool {  // PV_A(t), PV_B(t)
-                if (!wait_or_abort(&B.v_full[t & 1], (t >> 1) & 1, abort_flag, a.status)) return false;
-                if (!wait_or_abort(&B.p_full[0], t & 1, abort_flag, a.status)) return false;
+            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status) &&
+                      wait_or_abort(&B.k_full[0], 0, abort_flag, a.status);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc_commit(&B.k_empty[0]);
+            }
+            for (int t = 0; ok && t < n_kv; ++t) {
+                const bool last = t + 1 == n_kv;
+                const int t1 = t + 1;
+                ok = wait_or_abort(&B.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.status) &&
+                     wait_or_abort(&B.p_full[0], t & 1, abort_flag, a.status);
+                if (!ok) break;
                 tc_fence_after();
                 issue_pv(0, t);
-                if (!wait_or_abort(&B.p_full[1], t & 1, abort_flag, a.status)) return false;
+                if (last) {
+                    tc_commit(&B.o_done[0]);
+                } else {
+                    if (!(ok = wait_or_abort(&B.k_full[t1 % kKStages], (t1 / kKStages) & 1, abort_flag, a.status)))
+                        break;
+                    tc_fence_after();
+                    issue_s(0, t1);
+                }
+                if (!(ok = wait_or_abort(&B.p_full[1], t & 1, abort_flag, a.status))) break;
                 tc_fence_after();
                 issue_pv(1, t);
-                tc_commit(&B.v_empty[t & 1]);
-                return true;
-            };
-            for (int t = 0; ok && t < n_kv; ++t) {
-                if (!wait_or_abort(B.k_full, t & 1, abort_flag, a.status)) break;
-                if (t > 0 && !wait_or_abort(&B.s_free[0], (t - 1) & 1, abort_flag, a.status)) break;
-                tc_fence_after();
-                issue_s(0);
-                if (t > 0 && !wait_or_abort(&B.s_free[1], (t - 1) & 1, abort_flag, a.status)) break;
-                tc_fence_after();
-                issue_s(1);
-                tc_commit(B.k_empty);
-                if (t > 0 && !do_pv(t - 1)) { ok = false; break; }
+                tc_commit(&B.v_empty[t % kVStages]);
+                if (last) {
+                    tc_commit(&B.o_done[1]);
+                } else {
+                    issue_s(1, t1);
+                    tc_commit(&B.k_empty[t1 % kKStages]);
+                }
             }
-            if (ok) do_pv(n_kv - 1);
             // every MMA this thread issued has completed once `drain` flips
             tc_commit(B.drain);
             mbar_wait(B.drain, 0, a.status);
@@ -299,34 +336,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;        // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + x * 128, tO = tmem + 256 + x * 128;
+        const uint32_t tS = tmem + lane_base + x * 128, tO = tmem + lane_base + 256 + x * 128;
         const int pos_r = pos0 + x * kBM + r;     // absolute position of this row
         const int pos_first = pos0 + x * kBM;     // ... of the tile's first row
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
-        unsigned char* sP = smem + kOffP + x * kTileBytes;
         for (int t = 0; t < n_kv; ++t) {
             if (!warp_wait(&B.s_full[x], t & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
             uint32_t sv[kBN];
 #pragma unroll
             for (int i = 0; i < kBN / 32; ++i)
-                tmem_ld32(tS + lane_base + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[i * 32]));
+                tmem_ld32(tS + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[i * 32]));
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&B.s_free[x]);
             // causal mask: keys past this row's position (only tiles that reach
             // beyond the tile's first row can have any)
-            const int lim = (t * kBN + kBN - 1 > pos_first) ? pos_r - t * kBN : kBN - 1;  // last visible column
-            float mx = -INFINITY;
+            if (t * kBN + kBN - 1 > pos_first) {
+                const int lim = pos_r - t * kBN;  // last visible column
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) {
-                const float v = i <= lim ? __uint_as_float(sv[i]) : -INFINITY;
-                sv[i] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+                for (int i = 0; i < kBN; ++i)
+                    if (i > lim) sv[i] = __float_as_uint(-INFINITY);
             }
-            const float m_tile = mx * sl2;
+            float m4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m4[u] = fmaxf(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1]));
+#pragma unroll
+            for (int i = 8; i < kBN; i += 8)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    m4[u] = max3(m4[u], __uint_as_float(sv[i + 2 * u]), __uint_as_float(sv[i + 2 * u + 1]));
+            const float m_tile = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
             float alpha = 1.f;
             bool rescale = false;
             if (m_used == -INFINITY) {
@@ -336,67 +376,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = m_tile;
                 rescale = true;
             }
-            // P = 2^(s*scale*log2e - m) as bf16; a row with no visible key yet
-            // subtracts +inf so every p is 0
+            // P = 2^(s*scale*log2e - m) as bf16, into S_x's first 64 columns; a
+            // row with no visible key yet subtracts +inf so every p is 0
             const float msub = m_used == -INFINITY ? INFINITY : m_used;
-            uint32_t pk2[kBN / 2];
-            float rs0 = 0.f, rs1 = 0.f;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < kBN / 2; ++i) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * i]), sl2, -msub));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * i + 1]), sl2, -msub));
-                const uint32_t w = pack_bf16_rn(p0, p1);
-                pk2[i] = w;
-                rs0 += bf16lo(w);  // sum what the MMA will actually use
-                rs1 += bf16hi(w);
+            for (int h32 = 0; h32 < 2; ++h32) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int e = h32 * 64 + 2 * i;
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -msub));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -msub));
+                    const uint32_t w = pack_bf16_rn(p0, p1);
+                    pk[i] = w;
+                    rs[(i & 1) * 2] += bf16lo(w);  // sum what the MMA will actually use
+                    rs[(i & 1) * 2 + 1] += bf16hi(w);
+                }
+                tmem_st32(tS + h32 * 32, pk);
             }
-            lsum = lsum * alpha + (rs0 + rs1);
-            if (t > 0 && !warp_wait(&B.pv_done[x], (t - 1) & 1, abort_flag, a.status)) { ok = false; break; }
-            // tcgen05.ld/st are warp-collective: the whole warp rescales if
-            // any of its rows must (alpha is 1 for the others)
+            lsum = lsum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+            // O_x: PV_x(t-1) completed before S_x(t) was reported.  tcgen05.ld/st
+            // are warp-collective: the whole warp rescales if any of its rows
+            // must (alpha is 1 for the others)
             if (__any_sync(0xffffffffu, rescale && t > 0)) {
-                tc_fence_after();
 #pragma unroll
                 for (int i = 0; i < kHD / 32; ++i) {
                     uint32_t v[32];
-                    tmem_ld32(tO + lane_base + i * 32, v);
+                    tmem_ld32(tO + i * 32, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(tO + lane_base + i * 32, v);
+                    tmem_st32(tO + i * 32, v);
                 }
-                tmem_st_wait();
             }
             // keys past the end of the sequence: V rows must be zero (stale
             // cache slots may hold anything, and 0 * NaN is NaN).  Tile A's
             // warps do it; PV_B(t) is issued after PV_A(t), after their signal.
             if (x == 0 && (t + 1) * kBN > seq_len) {
-                if (!warp_wait(&B.v_full[t & 1], (t >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                if (!warp_wait(&B.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
                 if (t * kBN + r >= seq_len) {
-                    unsigned char* vrow = smem + kOffV + (t & 1) * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+                    unsigned char* vrow = smem + kOffV + (t % kVStages) * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                     for (int pnl = 0; pnl < 2; ++pnl)
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch)
                             *reinterpret_cast<uint4*>(vrow + pnl * kPanel + ch * 16) = make_uint4(0, 0, 0, 0);
                 }
+                fence_async_smem();
             }
-            // row r of P: 2 panels x 8 chunks of 16 bytes, chunk index XOR (r % 8)
-            unsigned char* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-            for (int pnl = 0; pnl < 2; ++pnl)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int w0 = pnl * 32 + ch * 4;
-                    *reinterpret_cast<uint4*>(prow + pnl * kPanel + ((ch ^ (r & 7)) << 4)) =
-                        make_uint4(pk2[w0], pk2[w0 + 1], pk2[w0 + 2], pk2[w0 + 3]);
-                }
-            fence_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&B.p_full[x]);
         }
         // epilogue: O / l -> bf16 rows of out
-        if (ok && warp_wait(&B.pv_done[x], (n_kv - 1) & 1, abort_flag, a.status)) {
+        if (ok && warp_wait(&B.o_done[x], 0, abort_flag, a.status)) {
             tc_fence_after();
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             const int rr = x * kBM + r;  // row of the 256
@@ -404,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kHD / 32; ++i) {
                 uint32_t v[32];
-                tmem_ld32(tO + lane_base + i * 32, v);
+                tmem_ld32(tO + i * 32, v);
                 tmem_ld_wait();
                 if (rr < rows) {
 #pragma unroll
