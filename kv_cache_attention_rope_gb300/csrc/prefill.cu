@@ -120,6 +120,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// One lane of the (converged) warp is elected: it alone issues tensor-core
+// instructions, while the warp's uniform values stay in uniform registers.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+    return pred != 0;
+}
+
 // One CTA: query rows [256 qt, 256 qt + 256) of chunk c, head j, as tiles A
 // (first 128 rows) and B (next 128), both against the same K/V stream.
 __global__ void __launch_bounds__(kThreads, 1)
@@ -276,66 +285,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ================================ MMA issuer =================================
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kHD, true);
-            auto issue_s = [&](int x, int t) {  // S_x = Q_x K_t^T
-                const uint32_t sQ = smem_addr(smem + kOffQ + x * kTileBytes);
-                const uint32_t sK = smem_addr(smem + kOffK + (t % kKStages) * kTileBytes);
+        // The whole warp runs the schedule (waits agreed by the warp) and one
+        // elected lane issues.  Operand descriptors are built once: a stage or
+        // k-step only adds (byte offset >> 4) to the start-address field, which
+        // cannot carry out of it (shared-memory offsets stay below 256 KB).  A
+        // lean issue loop matters: at N = 128 an MMA lasts ~64 cycles, and
+        // rebuilding descriptors per MMA made issue, not the tensor core, the
+        // bottleneck.
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kHD, true);
+        const uint32_t sbase = smem_addr(smem);
+        const uint64_t dQ = umma_desc_sw128(sbase + kOffQ, 16, 1024);    // Q_x: + x * kTileBytes
+        const uint64_t dK = umma_desc_sw128(sbase + kOffK, 16, 2048);    // K stage s: + s * kTileBytes
+        const uint64_t dV = umma_desc_sw128(sbase + kOffV, 1024, 2048);  // V stage s: + s * kTileBytes
+        constexpr uint64_t kTileStep = kTileBytes >> 4;
+        auto issue_s = [&](int x, int t) {  // S_x = Q_x K_t^T
+            if (elect_one()) {
+                const uint64_t q = dQ + x * kTileStep, kd = dK + (t % kKStages) * kTileStep;
+                const uint32_t d = tmem + x * 128;
 #pragma unroll
-                for (int k = 0; k < kHD / 16; ++k) {
-                    const uint32_t koff = (k & 3) * 32;  // 16 columns inside the 128-byte swizzle atom
-                    tc_mma_f16(tmem + x * 128, umma_desc_sw128(sQ + (k >> 2) * kPanel + koff, 16, 1024),
-                               umma_desc_sw128(sK + (k >> 2) * 1024 + koff, 16, 2048), idesc_s, k > 0);
-                }
+                for (int k = 0; k < kHD / 16; ++k)  // k-step: 16 columns, 32 B inside the 128-byte atom
+                    tc_mma_f16(d, q + (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4),
+                               kd + (uint64_t)(((k >> 2) * 1024 + (k & 3) * 32) >> 4), idesc_s, k > 0);
                 tc_commit(&B.s_full[x]);
-            };
-            auto issue_pv = [&](int x, int t) {  // O_x += P_x V_t, P_x in S_x's first 64 columns
-                const uint32_t sV = smem_addr(smem + kOffV + (t % kVStages) * kTileBytes);
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int x, int t, bool last) {  // O_x += P_x V_t, P_x in S_x's first 64 columns
+            if (elect_one()) {
+                const uint64_t vd = dV + (t % kVStages) * kTileStep;
+                const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k)
-                    tc_mma_f16_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8,
-                                  umma_desc_sw128(sV + k * 2 * 2048, 1024, 2048), idesc_o, (t > 0 || k > 0));
-            };
-            bool ok = wait_or_abort(B.q_full, 0, abort_flag, a.status) &&
-                      wait_or_abort(&B.k_full[0], 0, abort_flag, a.status);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                issue_s(1, 0);
-                tc_commit(&B.k_empty[0]);
+                for (int k = 0; k < kBN / 16; ++k)  // k-step: 16 keys = two 8-key groups
+                    tc_mma_f16_ts(d, pa + k * 8, vd + (uint64_t)((k * 2 * 2048) >> 4), idesc_o, (t > 0 || k > 0));
+                if (x == 1) tc_commit(&B.v_empty[t % kVStages]);
+                if (last) tc_commit(&B.o_done[x]);
             }
-            for (int t = 0; ok && t < n_kv; ++t) {
-                const bool last = t + 1 == n_kv;
-                const int t1 = t + 1;
-                ok = wait_or_abort(&B.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.status) &&
-                     wait_or_abort(&B.p_full[0], t & 1, abort_flag, a.status);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, t);
-                if (last) {
-                    tc_commit(&B.o_done[0]);
-                } else {
-                    if (!(ok = wait_or_abort(&B.k_full[t1 % kKStages], (t1 / kKStages) & 1, abort_flag, a.status)))
-                        break;
-                    tc_fence_after();
-                    issue_s(0, t1);
-                }
-                if (!(ok = wait_or_abort(&B.p_full[1], t & 1, abort_flag, a.status))) break;
-                tc_fence_after();
-                issue_pv(1, t);
-                tc_commit(&B.v_empty[t % kVStages]);
-                if (last) {
-                    tc_commit(&B.o_done[1]);
-                } else {
-                    issue_s(1, t1);
-                    tc_commit(&B.k_empty[t1 % kKStages]);
-                }
-            }
-            // every MMA this thread issued has completed once `drain` flips
-            tc_commit(B.drain);
-            mbar_wait(B.drain, 0, a.status);
+            __syncwarp();
+        };
+        auto wait = [&](uint64_t* b, uint32_t parity) { return warp_wait(b, parity, abort_flag, a.status); };
+        bool ok = wait(B.q_full, 0) && wait(&B.k_full[0], 0);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0, 0);
+            issue_s(1, 0);
+            if (elect_one()) tc_commit(&B.k_empty[0]);
+            __syncwarp();
         }
+        for (int t = 0; ok && t < n_kv; ++t) {
+            const bool last = t + 1 == n_kv;
+            const int t1 = t + 1;
+            if (!(ok = wait(&B.v_full[t % kVStages], (t / kVStages) & 1) && wait(&B.p_full[0], t & 1))) break;
+            tc_fence_after();
+            issue_pv(0, t, last);
+            if (!last) {
+                if (!(ok = wait(&B.k_full[t1 % kKStages], (t1 / kKStages) & 1))) break;
+                tc_fence_after();
+                issue_s(0, t1);
+            }
+            if (!(ok = wait(&B.p_full[1], t & 1))) break;
+            tc_fence_after();
+            issue_pv(1, t, last);
+            if (!last) {
+                issue_s(1, t1);
+                if (elect_one()) tc_commit(&B.k_empty[t1 % kKStages]);
+                __syncwarp();
+            }
+        }
+        // every MMA this warp issued has completed once `drain` flips
+        if (elect_one()) tc_commit(B.drain);
+        __syncwarp();
+        mbar_wait(B.drain, 0, a.status);
     } else {
         // ============================ softmax / epilogue ============================
         const int x = (warp - 2) >> 2;            // tile A (0) or B (1)
