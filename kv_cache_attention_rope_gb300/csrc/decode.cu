@@ -46,34 +46,6 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMinPer = 4;  // fewest tiles in a CTA's range (flat mode)
 constexpr int kCtasPerSm = 3;  // residency the register and shared-memory budgets aim at
 
-// --------------------------------------------------------- packed f32x2 math
-
-__device__ __forceinline__ uint64_t pk(float lo, float hi)
-{
-    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-__device__ __forceinline__ float pk_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
-__device__ __forceinline__ float pk_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
-
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 // 16 bytes of cache elements -> f32x2 pairs (element 2i in the low half)
 template <bool kBF16>
 __device__ __forceinline__ void unpack16(const uint4& w, uint64_t* out)

@@ -13,7 +13,9 @@
 //  - warp 0 (one lane) streams with TMA tensor copies: both 128 x 128 bf16 Q
 //    tiles once, then 128-key K and V tiles (two stages each), each gathered
 //    as eight 16-token pages of the KV head straight from the block table,
-//    one 4 KB copy per page, 128-byte swizzled (the layout the MMA reads).
+//    one 4 KB copy per page, issued by the page's own lane (a single lane
+//    issuing the eight copies one after another was the slowest step of the
+//    whole pipeline), 128-byte swizzled (the layout the MMA reads).
 //    A K/V stage is laid out [8-key group][64-column panel][8 keys][128 B]:
 //    a page is then one contiguous 4 KB box of a 4-D view of the pool, and
 //    both MMA operand descriptors still see uniform strides (2 KB between
@@ -249,13 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
-            for (int g = 0; g < kBN / kPage; ++g) {
-                const int yg = __shfl_sync(0xffffffffu, y, g);
-                if (lane == 0 && ((pages >> g) & 1u)) {
-                    tma_load_4d(smem + kOffK + ks * kTileBytes + g * kPageBytes, &maps.k, 0, 0, 0, yg >> 3,
-                                &B.k_full[ks], pol_kv);
-                }
-            }
+            if (have)
+                tma_load_4d(smem + kOffK + ks * kTileBytes + lane * kPageBytes, &maps.k, 0, 0, 0, y >> 3,
+                            &B.k_full[ks], pol_kv);
             k_issued = t + 1;
             // V stage t % kVStages: free once PV_A and PV_B of tile t - kVStages are done
             const int vs = t % kVStages;
@@ -266,13 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
-            for (int g = 0; g < kBN / kPage; ++g) {
-                const int yg = __shfl_sync(0xffffffffu, y, g);
-                if (lane == 0 && ((pages >> g) & 1u)) {
-                    tma_load_4d(smem + kOffV + vs * kTileBytes + g * kPageBytes, &maps.v, 0, 0, 0, yg >> 3,
-                                &B.v_full[vs], pol_kv);
-                }
-            }
+            if (have)
+                tma_load_4d(smem + kOffV + vs * kTileBytes + lane * kPageBytes, &maps.v, 0, 0, 0, y >> 3,
+                            &B.v_full[vs], pol_kv);
             v_issued = t + 1;
         }
         // After an abort, let every armed copy land before the CTA can exit.
@@ -403,25 +397,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rescale = true;
             }
             // P = 2^(s*scale*log2e - m) as bf16, into S_x's first 64 columns; a
-            // row with no visible key yet subtracts +inf so every p is 0
+            // row with no visible key yet subtracts +inf so every p is 0.  Pairs
+            // go through packed f32x2 FMAs and adds; the row sum adds the fp32
+            // p (their bf16 roundings differ by < 2^-9 relative, at random).
             const float msub = m_used == -INFINITY ? INFINITY : m_used;
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t scale2 = pk(sl2, sl2), msub2 = pk(-msub, -msub);
+            uint64_t sum2[2] = {0, 0};
 #pragma unroll
             for (int h32 = 0; h32 < 2; ++h32) {
-                uint32_t pk[32];
+                uint32_t pw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int e = h32 * 64 + 2 * i;
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), sl2, -msub));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), sl2, -msub));
-                    const uint32_t w = pack_bf16_rn(p0, p1);
-                    pk[i] = w;
-                    rs[(i & 1) * 2] += bf16lo(w);  // sum what the MMA will actually use
-                    rs[(i & 1) * 2 + 1] += bf16hi(w);
+                    const uint64_t xx = ffma2(pk(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), scale2, msub2);
+                    const uint64_t pp = pk(fast_exp2(pk_lo(xx)), fast_exp2(pk_hi(xx)));
+                    pw[i] = pack_bf16_rn(pk_lo(pp), pk_hi(pp));
+                    sum2[i & 1] = fadd2(sum2[i & 1], pp);
                 }
-                tmem_st32(tS + h32 * 32, pk);
+                tmem_st32(tS + h32 * 32, pw);
             }
-            lsum = lsum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+            lsum = lsum * alpha + ((pk_lo(sum2[0]) + pk_hi(sum2[0])) + (pk_lo(sum2[1]) + pk_hi(sum2[1])));
             // O_x: PV_x(t-1) completed before S_x(t) was reported.  tcgen05.ld/st
             // are warp-collective: the whole warp rescales if any of its rows
             // must (alpha is 1 for the others)
