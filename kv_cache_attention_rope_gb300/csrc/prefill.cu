@@ -46,6 +46,7 @@
 //  - Every wait is bounded (1 s): a timeout records KVATTN_ERR_TIMEOUT, the
 //    roles stop waiting, drain their in-flight copies and MMAs, free TMEM and
 //    return.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -69,8 +70,12 @@ constexpr int kOffQ = 0;                   // Q_A, Q_B
 constexpr int kOffK = 2 * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack to align the base to 1 KB
+constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
+constexpr int kOffX = kOffBar + 256;  // softmax exchange: row maxima [2][2][128], row sums [2][2][128] (fp32)
+constexpr int kOffOrder = kOffX + 4096;  // work order: sorted pairs, tiles per pair (int32)
+constexpr int kMaxPairs = 1024;         // more (chunk, 256-row) pairs than this: unsorted order
+constexpr int kSmemBytes = kOffOrder + 2 * kMaxPairs * 4 + 1024;  // + slack to align the base to 1 KB
+static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit before the exchange area");
 
 struct Maps {
     CUtensorMap q;  // 3-D: (D, Hq, total_q), box (64, 1, 128)
@@ -80,6 +85,7 @@ struct Maps {
 
 struct Bars {
     uint64_t* q_full;
+    uint64_t* q_empty;  // every S MMA of the current item is done
     uint64_t* k_full;   // [kKStages]
     uint64_t* k_empty;  // [kKStages]
     uint64_t* v_full;   // [kVStages]
@@ -122,6 +128,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// Named barrier `id` over `nthreads` threads that also returns the AND of
+// every participant's `v` (bar.red.and).
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool v)
+{
+    uint32_t res;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(res)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return res != 0;
+}
+
 // One lane of the (converged) warp is elected: it alone issues tensor-core
 // instructions, while the warp's uniform values stay in uniform registers.
 __device__ __forceinline__ bool elect_one()
@@ -131,8 +151,65 @@ __device__ __forceinline__ bool elect_one()
     return pred != 0;
 }
 
-// One CTA: query rows [256 qt, 256 qt + 256) of chunk c, head j, as tiles A
-// (first 128 rows) and B (next 128), both against the same K/V stream.
+// One work item: query rows [256 qt, 256 qt + 256) of chunk c, query head j,
+// as tiles A (first 128 rows) and B (next 128) against the same K/V stream.
+struct Item {
+    int c, j, h;      // chunk, query head, KV head
+    int seq_len;      // prefix + chunk length
+    int rows;         // valid rows of the 256
+    int row0;         // first q row (token index)
+    int pos0;         // absolute position of row 0
+    int n_kv;         // 128-key tiles (0: nothing to do)
+};
+
+// Tiles of the (chunk, 256-row block) pair: the key range row 255 (or the
+// last row) sees; 0 when the block is past the chunk's end or the chunk's
+// metadata is out of range (recorded by make_item).
+__device__ __forceinline__ int pair_tiles(const PrefillArgs& a, int n_qt, int pair)
+{
+    const int c = pair / n_qt, qt = pair % n_qt;
+    const int q0 = a.cu_q_lens[c], qlen = a.cu_q_lens[c + 1] - q0, P = a.prefix_lens[c];
+    if (qt * 2 * kBM >= qlen) return 0;
+    if (qlen < 0 || P < 0 || qlen > a.max_q_len || q0 < 0 || q0 + qlen > a.total_q ||
+        (int64_t)(P + qlen) > (int64_t)a.max_blocks * a.block_size)
+        return 0;
+    const int rows = min(2 * kBM, qlen - qt * 2 * kBM);
+    return (P + qt * 2 * kBM + rows - 1) / kBN + 1;
+}
+
+__device__ __forceinline__ Item make_item(const PrefillArgs& a, int n_qt, int pair, int j, bool report)
+{
+    Item it;
+    it.c = pair / n_qt;
+    const int qt = pair % n_qt;
+    it.j = j;
+    it.h = j / (a.hq / a.hkv);
+    const int q0 = a.cu_q_lens[it.c], qlen = a.cu_q_lens[it.c + 1] - q0, P = a.prefix_lens[it.c];
+    it.seq_len = P + qlen;
+    it.n_kv = 0;
+    it.rows = it.row0 = it.pos0 = 0;
+    if (qt * 2 * kBM >= qlen) return it;  // nothing to do
+    if (qlen < 0 || P < 0 || qlen > a.max_q_len || q0 < 0 || q0 + qlen > a.total_q ||
+        (int64_t)it.seq_len > (int64_t)a.max_blocks * a.block_size) {
+        if (report) record_error(a.status, KVATTN_ERR_BAD_INDEX);
+        return it;
+    }
+    it.rows = min(2 * kBM, qlen - qt * 2 * kBM);
+    it.row0 = q0 + qt * 2 * kBM;
+    it.pos0 = P + qt * 2 * kBM;
+    it.n_kv = (it.pos0 + it.rows - 1) / kBN + 1;
+    return it;
+}
+
+// Persistent CTAs (one per SM).  Work items are (pair, head) with pairs in
+// descending order of KV tiles (every CTA ranks them identically in shared
+// memory; ties by index), heads innermost, so the query heads of one KV head
+// run side by side and share its pages through L2.  CTA k takes, in round r,
+// item r G + k for even r and r G + G - 1 - k for odd r (G CTAs): a snake
+// over the sorted list, which balances the long items against the short
+// ones without a global counter.  Pipeline state (stages, phases) runs on
+// across items, so the next item's Q, K, V and first S overlap the current
+// item's last tiles and epilogue.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ Maps maps, const int n_qt)
 {
@@ -143,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         uint64_t* b = bar;
         B.q_full = b; b += 1;
+        B.q_empty = b; b += 1;
         B.k_full = b; b += kKStages;
         B.k_empty = b; b += kKStages;
         B.v_full = b; b += kVStages;
@@ -154,31 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* order = reinterpret_cast<int*>(smem + kOffOrder);  // sorted pairs
+    int* plen = order + kMaxPairs;                          // tiles per pair
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int idx = blockIdx.x;
-    const int j = idx % a.hq;  // query head
-    idx /= a.hq;
-    const int qt = idx % n_qt;  // 256-row query block of the chunk
-    const int c = idx / n_qt;   // chunk
-    const int q0 = a.cu_q_lens[c];
-    const int qlen = a.cu_q_lens[c + 1] - q0;
-    const int P = a.prefix_lens[c];
-    if (qt * 2 * kBM >= qlen) return;  // the whole CTA: nothing to do
-    const int seq_len = P + qlen;
-    if (qlen < 0 || P < 0 || qlen > a.max_q_len || q0 < 0 || q0 + qlen > a.total_q ||
-        (int64_t)seq_len > (int64_t)a.max_blocks * a.block_size) {
-        if (threadIdx.x == 0) record_error(a.status, KVATTN_ERR_BAD_INDEX);
-        return;
+    const int n_pairs = a.num_chunks * n_qt;
+    const bool sorted = n_pairs <= kMaxPairs;
+    if (sorted) {
+        for (int i = threadIdx.x; i < n_pairs; i += kThreads) plen[i] = pair_tiles(a, n_qt, i);
     }
-    const int rows = min(2 * kBM, qlen - qt * 2 * kBM);  // valid rows of the 256
-    const int row0 = q0 + qt * 2 * kBM;                   // first q row (token index)
-    const int pos0 = P + qt * 2 * kBM;                    // absolute position of row 0
-    const int n_kv = (pos0 + rows - 1) / kBN + 1;
-    const int h = j / (a.hq / a.hkv);  // KV head
-
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 1);
+        mbar_init(B.q_empty, 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&B.k_full[s], 1);
             mbar_init(&B.k_empty[s], 1);
@@ -189,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&B.s_full[x], 1);
-            mbar_init(&B.p_full[x], 128);
+            mbar_init(&B.p_full[x], 256);
             mbar_init(&B.o_done[x], 1);
         }
         mbar_init(B.drain, 1);
@@ -197,85 +262,125 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
+    __syncthreads();
+    if (sorted) {  // rank = pairs with more tiles, or as many and a smaller index
+        for (int i = threadIdx.x; i < n_pairs; i += kThreads) {
+            const int li = plen[i];
+            int rank = 0;
+            for (int q = 0; q < n_pairs; ++q) {
+                const int lq = plen[q];
+                rank += (lq > li) || (lq == li && q < i);
+            }
+            order[rank] = i;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;  // S_A at +0, S_B at +128, O_A at +256, O_B at +384
+    const int n_items = n_pairs * a.hq;
+    const int G = gridDim.x, k_cta = blockIdx.x;
+    // i-th item of this CTA's sequence (-1 past the end)
+    auto item_index = [&](int r) -> int {
+        const int i = r * G + ((r & 1) ? G - 1 - k_cta : k_cta);
+        return i < n_items ? i : -1;
+    };
+    auto item_at = [&](int i, bool report) -> Item {
+        const int pr = i / a.hq;
+        return make_item(a, n_qt, sorted ? order[pr] : pr, i % a.hq, report);
+    };
 
     if (warp == 0) {
         // ================================ TMA producer ================================
         const uint64_t pol_q = l2_evict_first_policy();
         const uint64_t pol_kv = l2_evict_normal_policy();
-        int k_issued = 0, v_issued = 0;
         if (lane == 0) {
             tma_prefetch_map(&maps.q);
             tma_prefetch_map(&maps.k);
             tma_prefetch_map(&maps.v);
-            mbar_arrive_expect_tx(B.q_full, 2 * kTileBytes);
-            for (int x = 0; x < 2; ++x) {
-                tma_load_3d(smem + kOffQ + x * kTileBytes, &maps.q, 0, j, row0 + x * kBM, B.q_full, pol_q);
-                tma_load_3d(smem + kOffQ + x * kTileBytes + kPanel, &maps.q, 64, j, row0 + x * kBM, B.q_full,
-                            pol_q);
-            }
         }
-        const int32_t* trow = a.block_table + (int64_t)c * a.max_blocks;
-        // lane g < 8 loads the block id of page g of tile t (keys 128t + 16g ..)
-        auto fetch = [&](int t) -> int32_t {
-            const int key0 = t * kBN + lane * kPage;
-            return (lane < kBN / kPage && t < n_kv && key0 < seq_len) ? trow[key0 / a.block_size] : -1;
-        };
-        int32_t blk_next = fetch(0);
-        for (int t = 0; t < n_kv; ++t) {
-            const int32_t blk = blk_next;
-            blk_next = fetch(t + 1);  // in flight while this tile is issued
-            int y = 0;
-            bool have = false;
-            const int key0 = t * kBN + lane * kPage;
-            if (lane < kBN / kPage && key0 < seq_len) {
-                if (blk < 0 || blk >= a.num_blocks) {
-                    record_error(a.status, KVATTN_ERR_BAD_INDEX);
-                } else {
-                    y = (int)(((int64_t)blk * a.hkv + h) * a.block_size + key0 % a.block_size);
-                    have = true;
+        int g = 0, ii = 0;    // tiles and items started so far (this CTA)
+        int kg = 0, vg = 0;   // tiles whose K / V copies are armed
+        bool go = true;
+        for (int r = 0; go; ++r) {
+            const int i = item_index(r);
+            if (i < 0) break;
+            const Item it = item_at(i, lane == 0);
+            if (it.n_kv == 0) continue;
+            // Q tiles: free once every S MMA of the previous item is done
+            if (lane == 0) {
+                go = ii > 0 ? wait_or_abort(B.q_empty, (ii - 1) & 1, abort_flag, a.status) : !*abort_flag;
+                if (go) {
+                    mbar_arrive_expect_tx(B.q_full, 2 * kTileBytes);
+                    for (int x = 0; x < 2; ++x) {
+                        tma_load_3d(smem + kOffQ + x * kTileBytes, &maps.q, 0, it.j, it.row0 + x * kBM, B.q_full,
+                                    pol_q);
+                        tma_load_3d(smem + kOffQ + x * kTileBytes + kPanel, &maps.q, 64, it.j, it.row0 + x * kBM,
+                                    B.q_full, pol_q);
+                    }
                 }
             }
-            const unsigned pages = __ballot_sync(0xffffffffu, have);
-            const uint32_t bytes = (uint32_t)__popc(pages) * (uint32_t)kPageBytes;
-            // K stage t % kKStages: free once S_A and S_B of tile t - kKStages are done
-            const int ks = t % kKStages;
-            bool go = true;
-            if (lane == 0) {
-                go = t >= kKStages ? wait_or_abort(&B.k_empty[ks], ((t / kKStages) - 1) & 1, abort_flag, a.status)
-                                   : !*abort_flag;
-                if (go) mbar_arrive_expect_tx(&B.k_full[ks], bytes);
-            }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
-            if (have)
-                tma_load_4d(smem + kOffK + ks * kTileBytes + lane * kPageBytes, &maps.k, 0, 0, 0, y >> 3,
-                            &B.k_full[ks], pol_kv);
-            k_issued = t + 1;
-            // V stage t % kVStages: free once PV_A and PV_B of tile t - kVStages are done
-            const int vs = t % kVStages;
-            if (lane == 0) {
-                go = t >= kVStages ? wait_or_abort(&B.v_empty[vs], ((t / kVStages) - 1) & 1, abort_flag, a.status)
-                                   : !*abort_flag;
-                if (go) mbar_arrive_expect_tx(&B.v_full[vs], bytes);
+            ++ii;
+            const int32_t* trow = a.block_table + (int64_t)it.c * a.max_blocks;
+            // lane p < 8 loads the block id of page p of tile t (keys 128t + 16p ..)
+            auto fetch = [&](int t) -> int32_t {
+                const int key0 = t * kBN + lane * kPage;
+                return (lane < kBN / kPage && t < it.n_kv && key0 < it.seq_len) ? trow[key0 / a.block_size] : -1;
+            };
+            int32_t blk_next = fetch(0);
+            for (int t = 0; t < it.n_kv; ++t, ++g) {
+                const int32_t blk = blk_next;
+                blk_next = fetch(t + 1);  // in flight while this tile is issued
+                int y = 0;
+                bool have = false;
+                const int key0 = t * kBN + lane * kPage;
+                if (lane < kBN / kPage && key0 < it.seq_len) {
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        record_error(a.status, KVATTN_ERR_BAD_INDEX);
+                    } else {
+                        y = (int)(((int64_t)blk * a.hkv + it.h) * a.block_size + key0 % a.block_size);
+                        have = true;
+                    }
+                }
+                const unsigned pages = __ballot_sync(0xffffffffu, have);
+                const uint32_t bytes = (uint32_t)__popc(pages) * (uint32_t)kPageBytes;
+                // K stage g % kKStages: free once S_A and S_B of tile g - kKStages are done
+                const int ks = g % kKStages;
+                if (lane == 0) {
+                    go = g >= kKStages ? wait_or_abort(&B.k_empty[ks], ((g / kKStages) - 1) & 1, abort_flag, a.status)
+                                       : !*abort_flag;
+                    if (go) mbar_arrive_expect_tx(&B.k_full[ks], bytes);
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) break;
+                if (have)
+                    tma_load_4d(smem + kOffK + ks * kTileBytes + lane * kPageBytes, &maps.k, 0, 0, 0, y >> 3,
+                                &B.k_full[ks], pol_kv);
+                kg = g + 1;
+                // V stage g % kVStages: free once PV_A and PV_B of tile g - kVStages are done
+                const int vs = g % kVStages;
+                if (lane == 0) {
+                    go = g >= kVStages ? wait_or_abort(&B.v_empty[vs], ((g / kVStages) - 1) & 1, abort_flag, a.status)
+                                       : !*abort_flag;
+                    if (go) mbar_arrive_expect_tx(&B.v_full[vs], bytes);
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) break;
+                if (have)
+                    tma_load_4d(smem + kOffV + vs * kTileBytes + lane * kPageBytes, &maps.v, 0, 0, 0, y >> 3,
+                                &B.v_full[vs], pol_kv);
+                vg = g + 1;
             }
-            go = __shfl_sync(0xffffffffu, go, 0);
-            if (!go) break;
-            if (have)
-                tma_load_4d(smem + kOffV + vs * kTileBytes + lane * kPageBytes, &maps.v, 0, 0, 0, y >> 3,
-                            &B.v_full[vs], pol_kv);
-            v_issued = t + 1;
         }
         // After an abort, let every armed copy land before the CTA can exit.
         if (lane == 0 && *abort_flag) {
-            for (int t = max(0, k_issued - kKStages); t < k_issued; ++t)
+            for (int t = max(0, kg - kKStages); t < kg; ++t)
                 mbar_wait(&B.k_full[t % kKStages], (t / kKStages) & 1, a.status);
-            for (int t = max(0, v_issued - kVStages); t < v_issued; ++t)
+            for (int t = max(0, vg - kVStages); t < vg; ++t)
                 mbar_wait(&B.v_full[t % kVStages], (t / kVStages) & 1, a.status);
-            mbar_wait(B.q_full, 0, a.status);
+            if (ii > 0) mbar_wait(B.q_full, (ii - 1) & 1, a.status);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer =================================
@@ -293,9 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dK = umma_desc_sw128(sbase + kOffK, 16, 2048);    // K stage s: + s * kTileBytes
         const uint64_t dV = umma_desc_sw128(sbase + kOffV, 1024, 2048);  // V stage s: + s * kTileBytes
         constexpr uint64_t kTileStep = kTileBytes >> 4;
-        auto issue_s = [&](int x, int t) {  // S_x = Q_x K_t^T
+        auto issue_s = [&](int x, int g) {  // S_x = Q_x K_g^T
             if (elect_one()) {
-                const uint64_t q = dQ + x * kTileStep, kd = dK + (t % kKStages) * kTileStep;
+                const uint64_t q = dQ + x * kTileStep, kd = dK + (g % kKStages) * kTileStep;
                 const uint32_t d = tmem + x * 128;
 #pragma unroll
                 for (int k = 0; k < kHD / 16; ++k)  // k-step: 16 columns, 32 B inside the 128-byte atom
@@ -305,177 +410,241 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int x, int t, bool last) {  // O_x += P_x V_t, P_x in S_x's first 64 columns
+        // O_x += P_x V_g, P_x in S_x's first 64 columns; the first tile of an
+        // item overwrites O_x (its previous item's epilogue read O_x before
+        // the softmax signalled this tile's P)
+        auto issue_pv = [&](int x, int g, bool first, bool last) {
             if (elect_one()) {
-                const uint64_t vd = dV + (t % kVStages) * kTileStep;
+                const uint64_t vd = dV + (g % kVStages) * kTileStep;
                 const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)  // k-step: 16 keys = two 8-key groups
-                    tc_mma_f16_ts(d, pa + k * 8, vd + (uint64_t)((k * 2 * 2048) >> 4), idesc_o, (t > 0 || k > 0));
-                if (x == 1) tc_commit(&B.v_empty[t % kVStages]);
+                    tc_mma_f16_ts(d, pa + k * 8, vd + (uint64_t)((k * 2 * 2048) >> 4), idesc_o, (!first || k > 0));
+                if (x == 1) tc_commit(&B.v_empty[g % kVStages]);
                 if (last) tc_commit(&B.o_done[x]);
             }
             __syncwarp();
         };
-        auto wait = [&](uint64_t* b, uint32_t parity) { return warp_wait(b, parity, abort_flag, a.status); };
-        bool ok = wait(B.q_full, 0) && wait(&B.k_full[0], 0);
-        if (ok) {
-            tc_fence_after();
-            issue_s(0, 0);
-            issue_s(1, 0);
-            if (elect_one()) tc_commit(&B.k_empty[0]);
+        auto commit = [&](uint64_t* b) {
+            if (elect_one()) tc_commit(b);
             __syncwarp();
-        }
-        for (int t = 0; ok && t < n_kv; ++t) {
-            const bool last = t + 1 == n_kv;
-            const int t1 = t + 1;
-            if (!(ok = wait(&B.v_full[t % kVStages], (t / kVStages) & 1) && wait(&B.p_full[0], t & 1))) break;
+        };
+        auto wait = [&](uint64_t* b, uint32_t parity) { return warp_wait(b, parity, abort_flag, a.status); };
+        int g = 0, ii = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int i = item_index(r);
+            if (i < 0) break;
+            const int n_kv = item_at(i, false).n_kv;
+            if (n_kv == 0) continue;
+            // order per tile t: PV_A(t) S_A(t+1) PV_B(t) S_B(t+1); S_x(t+1)
+            // overwrites S_x's columns after PV_x(t) has read P_x(t) from them
+            // (tensor operations of one thread run in issue order)
+            if (!(ok = wait(B.q_full, ii & 1) && wait(&B.k_full[g % kKStages], (g / kKStages) & 1))) break;
+            ++ii;
             tc_fence_after();
-            issue_pv(0, t, last);
-            if (!last) {
-                if (!(ok = wait(&B.k_full[t1 % kKStages], (t1 / kKStages) & 1))) break;
+            issue_s(0, g);
+            issue_s(1, g);
+            commit(&B.k_empty[g % kKStages]);
+            if (n_kv == 1) commit(B.q_empty);
+            for (int t = 0; t < n_kv; ++t, ++g) {
+                const bool last = t + 1 == n_kv;
+                const int g1 = g + 1;
+                if (!(ok = wait(&B.v_full[g % kVStages], (g / kVStages) & 1) && wait(&B.p_full[0], g & 1))) break;
                 tc_fence_after();
-                issue_s(0, t1);
-            }
-            if (!(ok = wait(&B.p_full[1], t & 1))) break;
-            tc_fence_after();
-            issue_pv(1, t, last);
-            if (!last) {
-                issue_s(1, t1);
-                if (elect_one()) tc_commit(&B.k_empty[t1 % kKStages]);
-                __syncwarp();
+                issue_pv(0, g, t == 0, last);
+                if (!last) {
+                    if (!(ok = wait(&B.k_full[g1 % kKStages], (g1 / kKStages) & 1))) break;
+                    tc_fence_after();
+                    issue_s(0, g1);
+                }
+                if (!(ok = wait(&B.p_full[1], g & 1))) break;
+                tc_fence_after();
+                issue_pv(1, g, t == 0, last);
+                if (!last) {
+                    issue_s(1, g1);
+                    commit(&B.k_empty[g1 % kKStages]);
+                    if (t + 2 == n_kv) commit(B.q_empty);  // the item's last S MMA
+                }
             }
         }
         // every MMA this warp issued has completed once `drain` flips
-        if (elect_one()) tc_commit(B.drain);
-        __syncwarp();
+        commit(B.drain);
         mbar_wait(B.drain, 0, a.status);
     } else {
         // ============================ softmax / epilogue ============================
-        const int x = (warp - 2) >> 2;            // tile A (0) or B (1)
+        // Warps 2-9 all work on whichever tile's S is due (A(t), B(t), A(t+1),
+        // ...): thread (quarter, lane) owns row r = 32 quarter + lane of the
+        // tile, warps 2-5 its columns 0..63 (half hf = 0) and warps 6-9 its
+        // columns 64..127 (hf = 1), so two warps per scheduler share each tile.
+        // The halves of a row agree on the row max through shared memory, one
+        // named barrier per tile; the barrier ANDs the waits' results, so a
+        // failed wait stops every softmax warp at the same point.
+        const int hf = (warp - 2) >> 2;
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;        // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base + x * 128, tO = tmem + lane_base + 256 + x * 128;
-        const int pos_r = pos0 + x * kBM + r;     // absolute position of this row
-        const int pos_first = pos0 + x * kBM;     // ... of the tile's first row
+        float* xchg = reinterpret_cast<float*>(smem + kOffX);  // [2 tile phases][2 halves][128 rows]
         const float sl2 = a.scale_log2;
-        float m_used = -INFINITY, lsum = 0.f;
+        int g = 0, ii = 0;
         bool ok = true;
-        for (int t = 0; t < n_kv; ++t) {
-            if (!warp_wait(&B.s_full[x], t & 1, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t sv[kBN];
+        for (int rr_ = 0; ok; ++rr_) {
+            const int i = item_index(rr_);
+            if (i < 0) break;
+            const Item it = item_at(i, false);
+            if (it.n_kv == 0) continue;
+            float m_used[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
+            for (int t = 0; ok && t < it.n_kv; ++t, ++g) {
 #pragma unroll
-            for (int i = 0; i < kBN / 32; ++i)
-                tmem_ld32(tS + i * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[i * 32]));
-            tmem_ld_wait();
-            // causal mask: keys past this row's position (only tiles that reach
-            // beyond the tile's first row can have any)
-            if (t * kBN + kBN - 1 > pos_first) {
-                const int lim = pos_r - t * kBN;  // last visible column
+                for (int x = 0; x < 2; ++x) {
+                    const uint32_t tS = tmem + lane_base + x * 128 + hf * 64;
+                    const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * 64;
+                    const int pos_r = it.pos0 + x * kBM + r;  // absolute position of this row
+                    const int pos_first = it.pos0 + x * kBM;  // ... of the tile's first row
+                    // keys past the end of the sequence: V rows must be zero (stale
+                    // cache slots may hold anything, and 0 * NaN is NaN).  Done in
+                    // tile A's phase; PV_B(t) is issued after PV_A(t).
+                    const bool zero_v = x == 0 && (t + 1) * kBN > it.seq_len;
+                    bool good = warp_wait(&B.s_full[x], g & 1, abort_flag, a.status);
+                    if (good && zero_v)
+                        good = warp_wait(&B.v_full[g % kVStages], (g / kVStages) & 1, abort_flag, a.status);
+                    uint32_t sv[64];
+                    float hm = -INFINITY;
+                    if (good) {
+                        tc_fence_after();
+                        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                        tmem_ld_wait();
+                        // causal mask: keys past this row's position (only tiles
+                        // that reach beyond the tile's first row can have any)
+                        if (t * kBN + kBN - 1 > pos_first) {
+                            const int lim = pos_r - t * kBN - hf * 64;  // last visible column of this half
 #pragma unroll
-                for (int i = 0; i < kBN; ++i)
-                    if (i > lim) sv[i] = __float_as_uint(-INFINITY);
-            }
-            float m4[4];
+                            for (int e = 0; e < 64; ++e)
+                                if (e > lim) sv[e] = __float_as_uint(-INFINITY);
+                        }
+                        float m4[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) m4[u] = fmaxf(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1]));
+                        for (int u = 0; u < 4; ++u)
+                            m4[u] = fmaxf(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1]));
 #pragma unroll
-            for (int i = 8; i < kBN; i += 8)
+                        for (int e = 8; e < 64; e += 8)
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    m4[u] = max3(m4[u], __uint_as_float(sv[i + 2 * u]), __uint_as_float(sv[i + 2 * u + 1]));
-            const float m_tile = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (m_used == -INFINITY) {
-                m_used = m_tile;
-            } else if (m_tile > m_used + 8.f) {
-                alpha = fast_exp2(m_used - m_tile);
-                m_used = m_tile;
-                rescale = true;
-            }
-            // P = 2^(s*scale*log2e - m) as bf16, into S_x's first 64 columns; a
-            // row with no visible key yet subtracts +inf so every p is 0.  Pairs
-            // go through packed f32x2 FMAs and adds; the row sum adds the fp32
-            // p (their bf16 roundings differ by < 2^-9 relative, at random).
-            const float msub = m_used == -INFINITY ? INFINITY : m_used;
-            const uint64_t scale2 = pk(sl2, sl2), msub2 = pk(-msub, -msub);
-            uint64_t sum2[2] = {0, 0};
+                            for (int u = 0; u < 4; ++u)
+                                m4[u] = max3(m4[u], __uint_as_float(sv[e + 2 * u]), __uint_as_float(sv[e + 2 * u + 1]));
+                        hm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    }
+                    float* slot = xchg + ((2 * g + x) & 1) * 256;
+                    slot[hf * 128 + r] = hm;
+                    if (!bar_and(1, 256, good)) {
+                        ok = false;
+                        break;
+                    }
+                    const float m_tile = fmaxf(hm, slot[(1 - hf) * 128 + r]) * sl2;
+                    float alpha = 1.f;
+                    bool rescale = false;
+                    if (m_used[x] == -INFINITY) {
+                        m_used[x] = m_tile;
+                    } else if (m_tile > m_used[x] + 8.f) {
+                        alpha = fast_exp2(m_used[x] - m_tile);
+                        m_used[x] = m_tile;
+                        rescale = true;
+                    }
+                    // P = 2^(s*scale*log2e - m) as bf16 into columns 32hf..32hf+31
+                    // of S_x (both halves have read their S before the barrier); a
+                    // row with no visible key yet subtracts +inf so every p is 0.
+                    // Pairs go through packed f32x2 FMAs and adds; the row sum
+                    // adds the fp32 p (their bf16 roundings differ by < 2^-9
+                    // relative, at random).
+                    const float msub = m_used[x] == -INFINITY ? INFINITY : m_used[x];
+                    const uint64_t scale2 = pk(sl2, sl2), msub2 = pk(-msub, -msub);
+                    uint64_t sum2[2] = {0, 0};
+                    uint32_t pw[32];
 #pragma unroll
-            for (int h32 = 0; h32 < 2; ++h32) {
-                uint32_t pw[32];
+                    for (int e = 0; e < 32; ++e) {
+                        const uint64_t xx =
+                            ffma2(pk(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), scale2, msub2);
+                        const uint64_t pp = pk(fast_exp2(pk_lo(xx)), fast_exp2(pk_hi(xx)));
+                        pw[e] = pack_bf16_rn(pk_lo(pp), pk_hi(pp));
+                        sum2[e & 1] = fadd2(sum2[e & 1], pp);
+                    }
+                    tmem_st32(tmem + lane_base + x * 128 + hf * 32, pw);
+                    lsum[x] = lsum[x] * alpha + ((pk_lo(sum2[0]) + pk_hi(sum2[0])) + (pk_lo(sum2[1]) + pk_hi(sum2[1])));
+                    // O_x (this half's 64 columns): PV_x(t-1) completed before
+                    // S_x(t) was reported.  tcgen05.ld/st are warp-collective: the
+                    // whole warp rescales if any of its rows must (alpha is 1 for
+                    // the others)
+                    if (__any_sync(0xffffffffu, rescale && t > 0)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int e = h32 * 64 + 2 * i;
-                    const uint64_t xx = ffma2(pk(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), scale2, msub2);
-                    const uint64_t pp = pk(fast_exp2(pk_lo(xx)), fast_exp2(pk_hi(xx)));
-                    pw[i] = pack_bf16_rn(pk_lo(pp), pk_hi(pp));
-                    sum2[i & 1] = fadd2(sum2[i & 1], pp);
+                        for (int q = 0; q < 2; ++q) {
+                            uint32_t v[32];
+                            tmem_ld32(tO + q * 32, v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            tmem_st32(tO + q * 32, v);
+                        }
+                    }
+                    if (zero_v) {
+                        if (t * kBN + r >= it.seq_len) {
+                            unsigned char* vrow = smem + kOffV + (g % kVStages) * kTileBytes + (r >> 3) * 2048 +
+                                                  hf * 1024 + (r & 7) * 128;
+#pragma unroll
+                            for (int ch = 0; ch < 8; ++ch)
+                                *reinterpret_cast<uint4*>(vrow + ch * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_async_smem();
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&B.p_full[x]);
                 }
-                tmem_st32(tS + h32 * 32, pw);
             }
-            lsum = lsum * alpha + ((pk_lo(sum2[0]) + pk_hi(sum2[0])) + (pk_lo(sum2[1]) + pk_hi(sum2[1])));
-            // O_x: PV_x(t-1) completed before S_x(t) was reported.  tcgen05.ld/st
-            // are warp-collective: the whole warp rescales if any of its rows
-            // must (alpha is 1 for the others)
-            if (__any_sync(0xffffffffu, rescale && t > 0)) {
+            if (!ok) break;
+            // epilogue: O / l -> bf16 rows of out, half hf writing columns
+            // 64hf..64hf+63.  The O reads complete before this item's last
+            // arrivals are followed by the next item's first P, which is what
+            // lets the next item's first P.V overwrite O.
+            const bool good = warp_wait(&B.o_done[0], ii & 1, abort_flag, a.status) &&
+                              warp_wait(&B.o_done[1], ii & 1, abort_flag, a.status);
+            ++ii;
+            float* lx = xchg + 512;  // [2 halves][2 tiles][128 rows]
+            lx[(hf * 2 + 0) * 128 + r] = lsum[0];
+            lx[(hf * 2 + 1) * 128 + r] = lsum[1];
+            if (!bar_and(1, 256, good)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < kHD / 32; ++i) {
+            for (int x = 0; x < 2; ++x) {
+                const float l = lsum[x] + lx[((1 - hf) * 2 + x) * 128 + r];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int row = x * kBM + r;  // row of the 256
+                __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                      ((int64_t)(it.row0 + row) * a.hq + it.j) * kHD + hf * 64;
+                const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * 64;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
                     uint32_t v[32];
-                    tmem_ld32(tO + i * 32, v);
+                    tmem_ld32(tO + q * 32, v);
                     tmem_ld_wait();
+                    if (row < it.rows) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(tO + i * 32, v);
-                }
-            }
-            // keys past the end of the sequence: V rows must be zero (stale
-            // cache slots may hold anything, and 0 * NaN is NaN).  Tile A's
-            // warps do it; PV_B(t) is issued after PV_A(t), after their signal.
-            if (x == 0 && (t + 1) * kBN > seq_len) {
-                if (!warp_wait(&B.v_full[t % kVStages], (t / kVStages) & 1, abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-                if (t * kBN + r >= seq_len) {
-                    unsigned char* vrow = smem + kOffV + (t % kVStages) * kTileBytes + (r >> 3) * 2048 + (r & 7) * 128;
-#pragma unroll
-                    for (int pnl = 0; pnl < 2; ++pnl)
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            *reinterpret_cast<uint4*>(vrow + pnl * 1024 + ch * 16) = make_uint4(0, 0, 0, 0);
-                }
-                fence_async_smem();
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&B.p_full[x]);
-        }
-        // epilogue: O / l -> bf16 rows of out
-        if (ok && warp_wait(&B.o_done[x], 0, abort_flag, a.status)) {
-            tc_fence_after();
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const int rr = x * kBM + r;  // row of the 256
-            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((int64_t)(row0 + rr) * a.hq + j) * kHD;
-#pragma unroll
-            for (int i = 0; i < kHD / 32; ++i) {
-                uint32_t v[32];
-                tmem_ld32(tO + i * 32, v);
-                tmem_ld_wait();
-                if (rr < rows) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16_rn(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                        w.y = pack_bf16_rn(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                        w.z = pack_bf16_rn(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                        w.w = pack_bf16_rn(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + i * 32 + e) = w;
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 w;
+                            w.x = pack_bf16_rn(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+                            w.y = pack_bf16_rn(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                            w.z = pack_bf16_rn(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                            w.w = pack_bf16_rn(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + q * 32 + e) = w;
+                        }
                     }
                 }
             }
+            // the lsum exchange area is rewritten by the next epilogue only
+            // after the next item's tile barriers, which every thread reaches
+            // after its reads here
         }
     }
     tc_fence_before();
@@ -555,9 +724,10 @@ kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
     });
     if (attr_err != cudaSuccess) return KVATTN_ERR_CUDA;
     const int n_qt = (a.max_q_len + 2 * kBM - 1) / (2 * kBM);
-    const int64_t grid = (int64_t)a.num_chunks * n_qt * a.hq;
-    if (grid <= 0) return KVATTN_OK;
-    if (grid > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
+    const int64_t items = (int64_t)a.num_chunks * n_qt * a.hq;
+    if (items <= 0) return KVATTN_OK;
+    if (items > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
+    const int64_t grid = std::min<int64_t>(items, num_sms());  // persistent: one CTA per SM
     prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, maps, n_qt);
     return cuda_status(cudaGetLastError());
 }

@@ -68,3 +68,25 @@ def test_c5_chunks_sampled_rows(kvattn_lib):
     case = PrefillCase(32, 8, [int(pre[i]) for i in idx], [512, 512], seed=5)
     rows = np.arange(0, 1024, 13)
     _check(kvattn_lib, case, rows=rows, what="c5 chunks")
+
+
+def test_persistent_schedule_many_items(kvattn_lib):
+    """More work items (chunk x 256-row block x head: 384) than SMs, of mixed
+    lengths and with empty blocks (chunks of 256 rows or fewer), so each
+    persistent CTA runs several items back to back in length order."""
+    prefixes = [3000, 0, 700, 1500, 64, 2222]
+    qlens = [512, 300, 17, 512, 256, 1]
+    case = PrefillCase(32, 8, prefixes, qlens, seed=6)
+    rows = np.arange(0, int(sum(qlens)), 7)
+    _check(kvattn_lib, case, rows=rows, what="persistent schedule")
+
+
+def test_unsorted_schedule_many_chunks(kvattn_lib):
+    """1100 one-token chunks: more (chunk, 256-row block) pairs than the
+    kernel ranks in shared memory, so items run in launch order."""
+    g = np.random.default_rng(7)
+    n = 1100
+    prefixes = [int(p) for p in g.integers(0, 200, n)]
+    case = PrefillCase(4, 1, prefixes, [1] * n, seed=7)
+    rows = np.arange(0, n, 11)
+    _check(kvattn_lib, case, rows=rows, what="unsorted schedule")
