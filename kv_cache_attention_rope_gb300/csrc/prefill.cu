@@ -8,8 +8,9 @@
 // holds the chunk's own keys.  The online softmax (running max and sum, the
 // accumulated output rescaled when the max grows) tiles the key axis.
 //
-// How (GB300 design), one CTA per (chunk, 256 query rows, query head), the
-// rows split into two 128-row tiles A and B that share one K/V stream:
+// How (GB300 design): persistent CTAs, one per SM, each running a sorted
+// share of the work items (chunk, 256 query rows, query head); an item's rows
+// are two 128-row tiles A and B that share one K/V stream:
 //  - warp 0 (one lane) streams with TMA tensor copies: both 128 x 128 bf16 Q
 //    tiles once, then 128-key K and V tiles (two stages each), each gathered
 //    as eight 16-token pages of the KV head straight from the block table,
@@ -23,7 +24,7 @@
 //    4 KB box instead of two 2 KB boxes per page) cut the kernel's time by a
 //    quarter: with 32 small copies per tile the stream was bound by copies
 //    issued, not by bytes.
-//  - warp 1 (one lane) issues the MMAs: S_x = Q_x K^T (M = N = 128, K = 128,
+//  - warp 1 (one elected lane) issues the MMAs: S_x = Q_x K^T (M = N = 128, K = 128,
 //    both operands in shared memory) and O_x += P_x V (P_x read from TMEM,
 //    V an MN-major shared-memory operand), x = A, B.  TMEM (512 columns)
 //    holds S_A, S_B, O_A, O_B; P_x (bf16, 64 columns) overwrites the first
@@ -37,12 +38,13 @@
 //    S_B(j+1) (ping-pong).  Completion is signalled with tcgen05.commit on
 //    mbarriers; a commit covers every earlier MMA of the thread, so when
 //    S_x(j+1) is reported done, PV_x(j) is too and O_x may be rescaled.
-//  - warps 2-5 (tile A) and 6-9 (tile B) own one query row per thread
-//    (= TMEM lane): load the row of S from TMEM, apply the causal mask on
-//    diagonal tiles, keep the running max (raised only when it grows by more
-//    than 2^8, which bounds p by 256 and keeps the O rescale rare), write P
-//    as bf16 into TMEM for the next MMA, and finally read O, divide by the
-//    row sum and store bf16.
+//  - warps 2-9 run the softmax of whichever tile is due, two threads per
+//    query row (= TMEM lane), one per 64-column half: load the half row of S
+//    from TMEM, apply the causal mask on diagonal tiles, agree on the row max
+//    with the other half through shared memory, keep the running max (raised
+//    only when it grows by more than 2^8, which bounds p by 256 and keeps the
+//    O rescale rare), write P as bf16 into TMEM for the next MMA, and finally
+//    read O, divide by the row sum and store bf16.
 //  - Every wait is bounded (1 s): a timeout records KVATTN_ERR_TIMEOUT, the
 //    roles stop waiting, drain their in-flight copies and MMAs, free TMEM and
 //    return.
