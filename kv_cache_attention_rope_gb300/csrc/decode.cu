@@ -33,9 +33,10 @@
 //    KVATTN_ERR_TIMEOUT and drains without further waiting.
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
-#include "kvattn_internal.cuh"
+#include "kvattn_tc.cuh"
 
 namespace kvattn {
 namespace {
@@ -44,7 +45,29 @@ constexpr int kTile = 16;  // tokens per tile
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMinPer = 4;  // fewest tiles in a CTA's range (flat mode)
-constexpr int kCtasPerSm = 3;  // residency the register and shared-memory budgets aim at
+// residency the register and shared-memory budgets aim at: 3 CTAs per SM on
+// the CUDA-core path; 2 on the tensor-core path, whose 16 x 8 accumulator
+// fragments need more registers and whose consumers need fewer warps
+template <bool kMma>
+constexpr int ctas_per_sm() { return kMma ? 2 : 3; }
+
+// Tensor maps of the K and V pools (tensor-core path).  Blocks of a multiple
+// of 16 tokens: one 4-D box per 16-token page, stage layout [8-row group]
+// [64-column panel][8 rows][128 B].  Otherwise (a contiguous cache of any
+// length): two 2-D boxes per page from any first row, layout [64-column
+// panel][16 rows][128 B].  The consumer only swaps two strides.
+struct PageMaps {
+    CUtensorMap k, v;
+};
+
+// 2^x (ex2.approx.ftz: a few ulp, far below the bf16 rounding P goes through
+// on the tensor-core path); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // 16 bytes of cache elements -> f32x2 pairs (element 2i in the low half)
 template <bool kBF16>
@@ -192,12 +215,16 @@ __device__ __forceinline__ bool len_ok(int L, const DecodeArgs& a)
     return L >= 0 && L <= a.max_seq_len && (int64_t)L <= (int64_t)a.max_blocks * a.block_size;
 }
 
-template <bool kBF16, int kD, int kGT>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(const __grid_constant__ DecodeArgs a,
+template <bool kBF16, int kD, int kGT, bool kMma, bool kRowBoxes>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_kernel(const __grid_constant__ DecodeArgs a,
+                                                                const __grid_constant__ PageMaps maps,
                                                                 const int stages)
 {
     using T = Traits<kBF16, kD, kGT>;
-    extern __shared__ __align__(1024) unsigned char smem[];
+    static_assert(!kMma || (kBF16 && kD == 128 && kGT <= 8), "tensor-core path: bf16, D = 128, <= 8 heads");
+    extern __shared__ unsigned char smem_raw[];
+    // 1 KB alignment: the tensor-core path's stages hold 128-byte-swizzled pages
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const SharedLayout SL = shared_layout<kBF16, kD, kGT>(stages, a.batch);
     unsigned char* ring = smem + SL.ring_off;
     float* merge = reinterpret_cast<float*>(smem + SL.merge_off);
@@ -328,12 +355,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(cons
                             const int nvalid = min(kTile, pc.len - tok);
                             const uint32_t bytes = (uint32_t)nvalid * kD * T::kE;
                             const int64_t row = (bj * a.hkv + h) * a.block_size + tok % a.block_size;
-                            const char* ksrc = (const char*)a.k_pool + row * kD * T::kE;
-                            const char* vsrc = (const char*)a.v_pool + row * kD * T::kE;
                             unsigned char* dst = ring + (size_t)stage * T::kStageBytes;
-                            mbar_arrive_expect_tx(&full[stage], 2 * bytes);
-                            bulk_load(dst, ksrc, bytes, &full[stage], policy);
-                            bulk_load(dst + T::kTileBytes, vsrc, bytes, &full[stage], policy);
+                            if constexpr (kMma) {
+                                // whole 16-row pages (rows past the sequence end are
+                                // masked out of S and zeroed in V by the consumer)
+                                mbar_arrive_expect_tx(&full[stage], 2 * T::kTileBytes);
+                                if constexpr (kRowBoxes) {
+                                    for (int pnl = 0; pnl < 2; ++pnl) {
+                                        tma_load_2d(dst + pnl * 2048, &maps.k, pnl * 64, (int)row, &full[stage], policy);
+                                        tma_load_2d(dst + T::kTileBytes + pnl * 2048, &maps.v, pnl * 64, (int)row,
+                                                    &full[stage], policy);
+                                    }
+                                } else {
+                                    tma_load_4d(dst, &maps.k, 0, 0, 0, (int)(row >> 3), &full[stage], policy);
+                                    tma_load_4d(dst + T::kTileBytes, &maps.v, 0, 0, 0, (int)(row >> 3), &full[stage],
+                                                policy);
+                                }
+                            } else {
+                                const char* ksrc = (const char*)a.k_pool + row * kD * T::kE;
+                                const char* vsrc = (const char*)a.v_pool + row * kD * T::kE;
+                                mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+                                bulk_load(dst, ksrc, bytes, &full[stage], policy);
+                                bulk_load(dst + T::kTileBytes, vsrc, bytes, &full[stage], policy);
+                            }
                         }
                     }
                     ++pos;
@@ -362,6 +406,119 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(cons
         const int h = pc.hh / nsub, hsub = pc.hh - h * nsub;
         const int ntiles = pc.t1 - pc.t0;
         const int qh0 = h * G + hsub * kGT;  // first query head of this segment
+        float* mw = merge + (size_t)warp * kGT * (kD + 2);
+        if constexpr (kMma) {
+            // ---- tensor-core path: S = Q K^T and O += P V as m16n8k16 MMAs
+            // with the query heads as rows (rows kGT..15 zero), so that the
+            // accumulator fragments of S are the A fragments of P.V
+            const int g4 = lane >> 2, q4 = lane & 3;  // fragment row, column pair
+            const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+            constexpr int gs = kRowBoxes ? 1024 : 2048, ps = kRowBoxes ? 2048 : 1024;  // group, panel strides
+            uint32_t qa[kD / 16][2];                  // Q rows g4: columns 2q4.. and 8+2q4.. of each k-step
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                qa[kk][0] = qa[kk][1] = 0u;
+                if (g4 < kGT) {
+                    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                        reinterpret_cast<const __nv_bfloat16*>(a.q) + ((int64_t)pc.b * hq + qh0 + g4) * kD + kk * 16);
+                    qa[kk][0] = qrow[q4];
+                    qa[kk][1] = qrow[4 + q4];
+                }
+            }
+            float o[kD / 8][4];
+#pragma unroll
+            for (int nd = 0; nd < kD / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+            float m_run = -INFINITY, lrun = 0.f;
+            const float sl2 = a.scale_log2;
+            for (int li = 0; li < ntiles; ++li) {
+                const uint32_t p = pos + li;
+                if ((int)(p % kConsumerWarps) != warp) continue;
+                const uint32_t stage = p % stages;
+                bool ready = !*abort_flag;
+                if (ready) ready = mbar_wait(&full[stage], (p / stages) & 1, a.status);
+                ready = __all_sync(0xffffffffu, ready);
+                if (!ready) {
+                    if (lane == 0) *abort_flag = 1;
+                    continue;
+                }
+                unsigned char* kst = ring + (size_t)stage * T::kStageBytes;
+                unsigned char* vst = kst + T::kTileBytes;
+                const int tok0 = (pc.t0 + li) * kTile;
+                const int nvalid = min(kTile, pc.len - tok0);
+                // page rows past the sequence end are stale: masked out of S,
+                // zeroed in V (their p is 0, but 0 * NaN would be NaN)
+                if (nvalid < kTile) {
+                    for (int idx = lane; idx < (kTile - nvalid) * 16; idx += 32) {
+                        const int row = nvalid + (idx >> 4), c = idx & 15;
+                        *reinterpret_cast<uint4*>(vst + (row >> 3) * gs + (c >> 3) * ps + (row & 7) * 128 +
+                                                  (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
+                // 16-byte chunk c of row r at chunk (c ^ r) of its 128 B (r = row mod 8)
+                const uint32_t kb = smem_addr(kst), vb = smem_addr(vst);
+                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-7, 8-15
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    // matrices (tokens 0-7, chunk 2kk), (0-7, 2kk+1), (8-15, 2kk), (8-15, 2kk+1)
+                    const int c = 2 * kk + (mi & 1), grp = mi >> 1;
+                    uint32_t b[4];
+                    ldmatrix_x4(b, kb + grp * gs + (c >> 3) * ps + rr * 128 + (((c & 7) ^ rr) << 4));
+                    mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b[0], b[1]);
+                    mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b[2], b[3]);
+                }
+                // row g4: tokens 2q4, 2q4+1 (s0) and 8+2q4, 9+2q4 (s1), in log2 units
+                float x[4] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2};
+                if (2 * q4 >= nvalid) x[0] = -INFINITY;
+                if (2 * q4 + 1 >= nvalid) x[1] = -INFINITY;
+                if (2 * q4 + 8 >= nvalid) x[2] = -INFINITY;
+                if (2 * q4 + 9 >= nvalid) x[3] = -INFINITY;
+                float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+                // reference max, raised only when a tile's max exceeds it by
+                // more than 2^8 (p <= 256, rare rescale of O)
+                if (tmax > m_run + 8.f) {
+                    const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - tmax);
+                    m_run = tmax;
+                    lrun *= alpha;
+#pragma unroll
+                    for (int nd = 0; nd < kD / 8; ++nd) {
+                        o[nd][0] *= alpha;
+                        o[nd][1] *= alpha;
+                    }
+                }
+                const float p0 = fast_exp2(x[0] - m_run), p1 = fast_exp2(x[1] - m_run);
+                const float p2 = fast_exp2(x[2] - m_run), p3 = fast_exp2(x[3] - m_run);
+                lrun += (p0 + p1) + (p2 + p3);
+                const uint32_t pa0 = pack_bf16_rn(p0, p1), pa2 = pack_bf16_rn(p2, p3);
+#pragma unroll
+                for (int nd2 = 0; nd2 < kD / 16; ++nd2) {
+                    // V^T fragments: matrices (tokens 0-7, chunk 2nd2), (8-15, 2nd2), (0-7, 2nd2+1), (8-15, 2nd2+1)
+                    const int c = 2 * nd2 + (mi >> 1), grp = mi & 1;
+                    uint32_t b[4];
+                    ldmatrix_x4_trans(b, vb + grp * gs + (c >> 3) * ps + rr * 128 + (((c & 7) ^ rr) << 4));
+                    mma_bf16_16816(o[2 * nd2], pa0, 0u, pa2, 0u, b[0], b[1]);
+                    mma_bf16_16816(o[2 * nd2 + 1], pa0, 0u, pa2, 0u, b[2], b[3]);
+                }
+                if (nvalid < kTile) fence_async_smem();  // zeroed rows before the next copy into this stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+            }
+            pos += ntiles;
+            lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
+            lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
+            __syncwarp();
+            if (g4 < kGT) {
+#pragma unroll
+                for (int nd = 0; nd < kD / 8; ++nd)
+                    *reinterpret_cast<float2*>(mw + g4 * (kD + 2) + nd * 8 + 2 * q4) = make_float2(o[nd][0], o[nd][1]);
+                if (q4 == 0) {
+                    mw[g4 * (kD + 2) + kD] = m_run;
+                    mw[g4 * (kD + 2) + kD + 1] = lrun;
+                }
+            }
+        } else {
 
         // query slice of this lane (head g^hm in slot g), pre-scaled by scale*log2(e)
         uint64_t q2[kGT][T::kP];
@@ -527,7 +684,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(cons
         }
         // ---- write this warp's state (over its own probability buffer), merge the warps
         __syncwarp();
-        float* mw = merge + (size_t)warp * kGT * (kD + 2);
         if (grp == 0) {
 #pragma unroll
             for (int g = 0; g < kGT; ++g) {
@@ -547,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_split_kernel(cons
                 }
             }
         }
+        }  // CUDA-core path
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
         const bool direct = pc.nslots == 1;
         if (tid == 0 && pc.slot == 0 && a.nslots) a.nslots[(int64_t)pc.b * HH + pc.hh] = pc.nslots;
@@ -625,12 +782,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     }
 }
 
-template <bool kBF16, int kD, int kGT>
+template <bool kBF16, int kD, int kGT, bool kMma, bool kRowBoxes = false>
 kvattn_status run(const DecodeArgs& a, cudaStream_t s)
 {
     using T = Traits<kBF16, kD, kGT>;
+    PageMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    if constexpr (kMma) {
+        const int64_t rows = a.num_blocks * a.hkv * a.block_size;
+        if (!(kRowBoxes ? make_row_maps(a.k_pool, a.v_pool, rows, &maps.k, &maps.v)
+                        : make_page_maps(a.k_pool, a.v_pool, rows, &maps.k, &maps.v)))
+            return KVATTN_ERR_CUDA;
+    }
     // Ring depth: as many stages (up to 64 KB of them) as leave room for
-    // kCtasPerSm CTAs per SM, counting the per-block reserved shared memory.
+    // ctas_per_sm CTAs per SM, counting the per-block reserved shared memory.
     static int smem_sm = 0, smem_reserved = 0;
     if (!smem_sm) {
         int dev = 0;
@@ -644,28 +809,29 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
     // always consumed by warp s % kConsumerWarps, in order, which keeps every
     // mbarrier wait at most one phase away from the phase it names (parity
     // waits cannot tell phase u from phase u - 2).
-    const int fixed = shared_layout<kBF16, kD, kGT>(0, a.batch).bytes;
-    const int budget = smem_sm / kCtasPerSm - smem_reserved - fixed;
+    const int fixed = shared_layout<kBF16, kD, kGT>(0, a.batch).bytes + 1024;  // + base alignment slack
+    const int budget = smem_sm / ctas_per_sm<kMma>() - smem_reserved - fixed;
     int stages = std::min(65536 / T::kStageBytes, budget / T::kStageBytes);
     stages = std::max(kConsumerWarps, stages / kConsumerWarps * kConsumerWarps);
     const SharedLayout SL = shared_layout<kBF16, kD, kGT>(stages, a.batch);
-    auto kern = decode_split_kernel<kBF16, kD, kGT>;
+    const int smem_bytes = SL.bytes + 1024;
+    auto kern = decode_split_kernel<kBF16, kD, kGT, kMma, kRowBoxes>;
     static std::mutex mu;
     static int configured_smem = 0;
     {
         std::lock_guard<std::mutex> g(mu);
-        if (SL.bytes > configured_smem) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SL.bytes);
+        if (smem_bytes > configured_smem) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
             if (e != cudaSuccess) return KVATTN_ERR_CUDA;
-            configured_smem = SL.bytes;
+            configured_smem = smem_bytes;
         }
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, SL.bytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes) != cudaSuccess)
         return KVATTN_ERR_CUDA;
     per_sm = std::max(1, per_sm);
     const int grid = num_sms() * per_sm;
-    kern<<<grid, kThreads, SL.bytes, s>>>(a, stages);
+    kern<<<grid, kThreads, smem_bytes, s>>>(a, maps, stages);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return KVATTN_ERR_CUDA;
     if (a.splits > 1) {
@@ -707,8 +873,12 @@ kvattn_status launch_decode(const DecodeArgs& a, cudaStream_t s)
     const int G = a.hq / a.hkv;
     const bool bf16 = a.dtype == KVATTN_BF16;
     const int gt = G >= 4 ? 4 : G;
+    // bf16, D = 128, groups of 4 query heads per KV head: QK and PV on the
+    // tensor cores (tensor-map row coordinates are 32-bit)
+    if (bf16 && a.d == 128 && gt == 4 && a.num_blocks * a.hkv * a.block_size < ((int64_t)1 << 31))
+        return a.block_size % 16 == 0 ? run<true, 128, 4, true, false>(a, s) : run<true, 128, 4, true, true>(a, s);
 #define KVATTN_DECODE_CASE(BF, DD, GG) \
-    if (bf16 == BF && a.d == DD && gt == GG) return run<BF, DD, GG>(a, s);
+    if (bf16 == BF && a.d == DD && gt == GG) return run<BF, DD, GG, false>(a, s);
     KVATTN_DECODE_CASE(true, 128, 1)
     KVATTN_DECODE_CASE(true, 128, 2)
     KVATTN_DECODE_CASE(true, 128, 4)

@@ -142,6 +142,45 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// Host: tensor maps of a K and a V pool of bf16 rows of 128 elements (rows =
+// num_blocks * num_kv_heads * block_size, a multiple of 16) for one-box loads
+// of 16-row pages into the 128-byte-swizzled layout [8-row group][64-column
+// panel][8 rows][128 B]; load a page with tma_load_4d(dst, map, 0, 0, 0,
+// first_row / 8, ...).  False if the driver entry point or the encoding fails.
+bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
+// Host: the same pools as 2-D maps (128 columns, rows) with a 64 x 16 box:
+// two boxes (columns 0 and 64) load 16 rows from any first row into the
+// 128-byte-swizzled layout [64-column panel][16 rows][128 B].
+bool make_row_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
+
+// Warp-level MMA (m16n8k16, bf16 inputs, fp32 accumulate) and its fragment
+// loads from shared memory; layouts as in the PTX ISA description.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr)
+                 : "memory");
+}
+// d (16x8 fp32) += A (16x16 bf16: a0 rows 0-7 k 0-7, a1 rows 8-15 k 0-7, a2
+// rows 0-7 k 8-15, a3 rows 8-15 k 8-15) x B (16x8 bf16: b0 k 0-7, b1 k 8-15)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor core, TMA) after this fence.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

@@ -693,25 +693,45 @@ bool make_maps(const PrefillArgs& a, Maps& m)
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
-    // K and V pools as (64 columns, 8 rows, 2 panels, rows / 8): a box of
-    // (64, 8, 2, 2) is one 16-row page, landing as [group][panel][row][128 B]
-    const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.hkv * a.block_size;
-    const cuuint64_t dims[4] = {64, 8, 2, rows / 8};
-    const cuuint64_t strides[3] = {(cuuint64_t)kHD * 2, 128, (cuuint64_t)kHD * 2 * 8};
-    const cuuint32_t box[4] = {64, 8, 2, 2};
-    const cuuint32_t estr4[4] = {1, 1, 1, 1};
-    if (enc(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_pool), dims, strides, box, estr4,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
-    if (enc(&m.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_pool), dims, strides, box, estr4,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
-    return true;
+    return make_page_maps(a.k_pool, a.v_pool, (int64_t)a.num_blocks * a.hkv * a.block_size, &m.k, &m.v);
 }
 
 }  // namespace
+
+bool make_row_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v)
+{
+    EncodeTiled enc = encoder();
+    if (!enc || rows <= 0) return false;
+    // (128 columns, rows): a box of (64, 16) is one 64-column panel of 16 rows
+    const cuuint64_t dims[2] = {(cuuint64_t)kHD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHD * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int i = 0; i < 2; ++i)
+        if (enc(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(i ? v_pool : k_pool), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    return true;
+}
+
+bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v)
+{
+    EncodeTiled enc = encoder();
+    if (!enc || rows <= 0 || rows % 16) return false;
+    // (64 columns, 8 rows, 2 panels, rows / 8): a box of (64, 8, 2, 2) is one
+    // 16-row page, landing as [8-row group][64-column panel][row][128 B]
+    const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)rows / 8};
+    const cuuint64_t strides[3] = {(cuuint64_t)kHD * 2, 128, (cuuint64_t)kHD * 2 * 8};
+    const cuuint32_t box[4] = {64, 8, 2, 2};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    for (int i = 0; i < 2; ++i)
+        if (enc(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(i ? v_pool : k_pool), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    return true;
+}
 
 kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
 {
