@@ -12,15 +12,16 @@
 // of the input values.  The angle is reduced exactly: the rotation speed of
 // pair i is held as a 64-bit fixed-point count of turns per position
 // (round(theta_i / 2pi * 2^64)), so position * speed mod 2^64 is the angle's
-// fraction of a turn with no cancellation at large positions.  Fast path:
-// sincospif of that fraction and one fp32 fma per output, with a rigorous
-// error bound delta = 2^-20 (|x0| + |x1|); if both ends of [y - delta,
-// y + delta] round to the same bf16 value that value is the correctly rounded
-// result.  Otherwise (a fraction of a percent of the elements, mostly results
-// near zero or near a rounding boundary) the element is recomputed in
-// float-float arithmetic (about 44 bits) with a twiddle from quadrant and
-// 1/32-turn sector reduction plus short Taylor series.  fp32 outputs always
-// take the float-float path.
+// fraction of a turn with no cancellation at large positions.  Each CTA
+// computes its token's (cos, sin) of every pair once, in float-float (about
+// 44 bits, quadrant and 1/32-turn sector reduction plus short Taylor series),
+// into shared memory.  Fast path: the fp32-rounded twiddle, one packed
+// multiply and one packed fma per pair, with a rigorous error bound delta =
+// 2^-21 (|x0| + |x1|); if both ends of [y - delta, y + delta] round to the
+// same bf16 value that value is the correctly rounded result.  Otherwise (a
+// fraction of a percent of the elements, mostly results near zero or near a
+// rounding boundary) the pair is recomputed in float-float.  fp32 outputs
+// always take the float-float path.
 #include "kvattn_internal.cuh"
 
 namespace kvattn {
@@ -159,43 +160,20 @@ __device__ __forceinline__ void rotate_pair_ff(float x0, float x1, const float4&
     y1 = ff_add(ff_mul_f(s, x0), ff_mul_f(c, x1));
 }
 
-__device__ __forceinline__ uint64_t pk2(float lo, float hi)
-{
-    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// A pair's twiddle as packed operands: y = x0 * (c, s) + x1 * (-s, c), for the
-// high and the low float of the float-float (c, s).
+// A pair's twiddle as packed operands: y = x0 * (c, s) + x1 * (-s, c) with
+// the fp32 roundings of the float-float (c, s); the float-float value itself
+// stays in shared memory for the slow path.
 struct Twiddle2 {
-    uint64_t cs_hi, sc_hi, cs_lo, sc_lo;  // (c, s), (-s, c) for hi and lo
-    float4 ff;                            // (c_hi, c_lo, s_hi, s_lo) for the slow path
+    uint64_t cs, sc;  // (c, s), (-s, c)
+    const float4* ff; // (c_hi, c_lo, s_hi, s_lo)
 };
 
-__device__ __forceinline__ Twiddle2 make_twiddle2(const float4& t)
+__device__ __forceinline__ Twiddle2 make_twiddle2(const float4* t)
 {
+    const float4 v = *t;
     Twiddle2 w;
-    w.cs_hi = pk2(t.x, t.z);
-    w.sc_hi = pk2(-t.z, t.x);
-    w.cs_lo = pk2(t.y, t.w);
-    w.sc_lo = pk2(-t.w, t.y);
+    w.cs = pk(v.x, v.z);
+    w.sc = pk(-v.z, v.x);
     w.ff = t;
     return w;
 }
@@ -221,23 +199,21 @@ __device__ __forceinline__ bool rounding_safe(float y, float delta_x_2p24)
 }
 
 // Rotates the bf16 pair packed in `w` (low half = even element).
-// Fast path: y = x0 (c, s)_hi + x1 (-s, c)_hi + [x0 (c, s)_lo + x1 (-s, c)_lo]
-// in fp32; its error is at most 3 * 2^-24 (|x0| + |x1|) (three roundings of
-// terms bounded by |x0| + |x1|; the twiddle itself is good to ~2^-44), so with
-// delta = 2^-21 (|x0| + |x1|) a pattern that passes rounding_safe rounds to the
-// correctly rounded rotation.  Otherwise the pair is recomputed in
+// Fast path: y = fl(fl(x0 (c, s)) + x1 (-s, c)) with the fp32-rounded
+// twiddle, one packed multiply and one packed fma.  Its error is at most
+// 3 * 2^-24 (|x0| + |x1|): the twiddle's rounding (2^-24 of each term), the
+// product's and the fma's roundings (2^-24 of terms bounded by |x0| + |x1|).
+// With delta = 2^-21 (|x0| + |x1|) a pattern that passes rounding_safe rounds
+// to the correctly rounded rotation.  Otherwise the pair is recomputed in
 // float-float and rounded from there.
 __device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const Twiddle2& tw)
 {
     const float x0 = bf16lo(w), x1 = bf16hi(w);
-    const uint64_t xx0 = pk2(x0, x0), xx1 = pk2(x1, x1);
-    const uint64_t hi = ffma2(xx1, tw.sc_hi, fmul2(xx0, tw.cs_hi));
-    const uint64_t lo = ffma2(xx1, tw.sc_lo, fmul2(xx0, tw.cs_lo));
-    const uint64_t y = fadd2(hi, lo);
-    const float y0 = __uint_as_float((uint32_t)y), y1 = __uint_as_float((uint32_t)(y >> 32));
+    const uint64_t y = ffma2(pk(x1, x1), tw.sc, fmul2(pk(x0, x0), tw.cs));
+    const float y0 = pk_lo(y), y1 = pk_hi(y);
     const float dx = 8.0f * (fabsf(x0) + fabsf(x1));  // 2^24 * 2^-21 * (|x0| + |x1|)
     if (rounding_safe(y0, dx) && rounding_safe(y1, dx)) return pack_bf16_rn(y0, y1);
-    return rotate_bf16_word_slow(x0, x1, tw.ff);
+    return rotate_bf16_word_slow(x0, x1, *tw.ff);
 }
 
 template <bool kBF16, int kD>
@@ -296,7 +272,7 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
     __syncthreads();
     Twiddle2 tws[kPPV];
 #pragma unroll
-    for (int p = 0; p < kPPV; ++p) tws[p] = make_twiddle2(tw[dv * kPPV + p]);
+    for (int p = 0; p < kPPV; ++p) tws[p] = make_twiddle2(&tw[dv * kPPV + p]);
 
     for (int base = 0; base < nv; base += kMaxV) {
         if (base > 0) {
@@ -330,8 +306,8 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
                     x.w = rotate_bf16_word(x.w, tws[3]);
                 } else {
                     ff z0, z1, z2, z3;
-                    rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), tws[0].ff, z0, z1);
-                    rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), tws[1].ff, z2, z3);
+                    rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), *tws[0].ff, z0, z1);
+                    rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), *tws[1].ff, z2, z3);
                     x = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
                                    __float_as_uint(z3.hi));
                 }
