@@ -76,11 +76,13 @@ constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
 constexpr int kOffX = kOffBar + 256;  // softmax exchange: row maxima [2][2][128], row sums [2][2][128] (fp32)
 constexpr int kOffOrder = kOffX + 4096;  // work order: sorted pairs, tiles per pair (int32)
 constexpr int kMaxPairs = 1024;         // more (chunk, 256-row) pairs than this: unsorted order
-constexpr int kSmemBytes = kOffOrder + 2 * kMaxPairs * 4 + 1024;  // + slack to align the base to 1 KB
+constexpr int kOffStage = (kOffOrder + 2 * kMaxPairs * 4 + 1023) / 1024 * 1024;  // output staging, 2 KB per softmax warp
+constexpr int kSmemBytes = kOffStage + 8 * 2048 + 1024;  // + slack to align the base to 1 KB
 static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit before the exchange area");
 
 struct Maps {
     CUtensorMap q;  // 3-D: (D, Hq, total_q), box (64, 1, 128)
+    CUtensorMap o;  // 3-D: (D, Hq, total_q), box (32, 1, 32), 64-byte swizzle (output stores)
     CUtensorMap k;  // 4-D: (64 columns, 8 rows, 2 panels, rows / 8), box (64, 8, 2, 2)
     CUtensorMap v;
 };
@@ -487,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = quarter * 32 + lane;        // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         float* xchg = reinterpret_cast<float*>(smem + kOffX);  // [2 tile phases][2 halves][128 rows]
+        unsigned char* stage = smem + kOffStage + (warp - 2) * 2048;  // this warp's output staging tile
         const float sl2 = a.scale_log2;
         int g = 0, ii = 0;
         bool ok = true;
@@ -623,24 +626,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float l = lsum[x] + lx[((1 - hf) * 2 + x) * 128 + r];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 const int row = x * kBM + r;  // row of the 256
-                __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                      ((int64_t)(it.row0 + row) * a.hq + it.j) * kHD + hf * 64;
                 const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * 64;
+                // this warp's 32 rows all belong to the item: TMA store of a
+                // 32-row x 32-column box per chunk from a 64-byte-swizzled
+                // staging tile (rows past the item's end belong to other
+                // chunks and are never written: plain stores there)
+                const bool full = x * kBM + quarter * 32 + 32 <= it.rows;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t v[32];
                     tmem_ld32(tO + q * 32, v);
                     tmem_ld_wait();
-                    if (row < it.rows) {
+                    uint32_t w[16];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            uint4 w;
-                            w.x = pack_bf16_rn(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                            w.y = pack_bf16_rn(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                            w.z = pack_bf16_rn(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                            w.w = pack_bf16_rn(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + q * 32 + e) = w;
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16_rn(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+                    if (full) {
+                        // the previous box's source has been read before it is overwritten
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)  // 16-byte chunk c of row `lane` at chunk c ^ ((lane >> 1) & 3)
+                            *reinterpret_cast<uint4*>(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&maps.o, hf * 64 + q * 32, it.j, it.row0 + x * kBM + quarter * 32, stage);
+                            bulk_commit_group();
                         }
+                    } else if (row < it.rows) {
+                        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                              ((int64_t)(it.row0 + row) * a.hq + it.j) * kHD + hf * 64 + q * 32;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(orow + 8 * c) =
+                                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                     }
                 }
             }
@@ -648,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // after the next item's tile barriers, which every thread reaches
             // after its reads here
         }
+        if (lane == 0) bulk_wait_group0();  // output stores complete before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -690,6 +712,11 @@ bool make_maps(const PrefillArgs& a, Maps& m)
         const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
         if (enc(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+        const cuuint32_t obox[3] = {32, 1, 32};
+        if (enc(&m.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, obox, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
