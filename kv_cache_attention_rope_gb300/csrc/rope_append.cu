@@ -4,9 +4,11 @@
 // x[2i+1]) of a query/key head vector rotate by m*theta_i, theta_i =
 // base^(-2i/D), m = the token position.  "From-scratch AI inference engine"
 // page, section 3.2: the new token's K/V go to the cache index equal to that
-// same position.  One CTA per token: it rotates every q head in place, rotates
-// every k head into the cache slot and copies v into the cache slot, moving
-// 16-byte vectors (8 bf16 / 4 fp32 values).
+// same position.  Every q head is rotated in place, every k head rotated into
+// the cache slot and v copied into the cache slot, in 16-byte vectors (8 bf16
+// / 4 fp32 values).  Persistent CTAs stream the tokens through a shared-memory
+// ring (rope_append_pipe_kernel); a token too large for two ring stages takes
+// the one-CTA-per-token kernel (rope_append_kernel).
 //
 // Rounding.  A stored element is round-to-nearest-even of the exact rotation
 // of the input values.  The angle is reduced exactly: the rotation speed of
@@ -22,6 +24,9 @@
 // fraction of a percent of the elements, mostly results near zero or near a
 // rounding boundary) the pair is recomputed in float-float.  fp32 outputs
 // always take the float-float path.
+#include <algorithm>
+#include <mutex>
+
 #include "kvattn_internal.cuh"
 
 namespace kvattn {
@@ -143,12 +148,6 @@ __device__ __forceinline__ uint32_t rne_bf16_ff(ff y)
         return ((b & 0xffff0000u) + (away ? 0x10000u : 0u)) >> 16;
     }
     __nv_bfloat16 h = __float2bfloat16_rn(y.hi);
-    return (uint32_t)(*reinterpret_cast<uint16_t*>(&h));
-}
-
-__device__ __forceinline__ uint32_t bf16_bits(float x)
-{
-    __nv_bfloat16 h = __float2bfloat16_rn(x);
     return (uint32_t)(*reinterpret_cast<uint16_t*>(&h));
 }
 
@@ -317,18 +316,233 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
     }
 }
 
+// ------------------------------------------------------- pipelined variant
+//
+// Persistent CTAs, each taking tokens blockIdx.x, blockIdx.x + gridDim.x, ...
+// Warp 4 is the producer: per token one lane starts 1-D bulk copies of the
+// token's q, k and v rows into a ring stage, and while they fly the warp looks
+// up the token's cache slot and computes its float-float twiddles into the
+// same stage.  Warps 0-3 rotate from shared memory and write q back in place
+// and k, v to the cache slot.  A token's loads no longer wait for the previous
+// token's compute, so a CTA keeps several tokens' bytes in flight.
+// Stage layout: [header 16 B][twiddles, kPairs x 16 B][q row][k row][v row].
+constexpr int kPipeConsumers = 4;
+constexpr int kPipeThreads = (kPipeConsumers + 1) * 32;
+constexpr int kPipeMaxStages = 8;
+
+struct PipeHeader {
+    long long blk;  // cache block of the token; -1: invalid token (skipped)
+    int off;        // slot in the block
+    int pad;
+};
+
+template <bool kBF16, int kD>
+__global__ void __launch_bounds__(kPipeThreads) rope_append_pipe_kernel(const __grid_constant__ RopeArgs a,
+                                                                         const int stages, const int stage_bytes)
+{
+    constexpr int kPairs = kD / 2;
+    constexpr int kEPV = kBF16 ? 8 : 4;  // elements per 16-byte vector
+    constexpr int kVPH = kD / kEPV;      // vectors per head
+    constexpr int kPPV = kEPV / 2;       // pairs per vector
+    constexpr int kGroups = 128 / kVPH;  // consumer threads sharing one column slice
+    constexpr int kE = kBF16 ? 2 : 4;
+    constexpr int kTwBytes = kPairs * 16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float4 sector[5];
+    __shared__ uint64_t bars[2 * kPipeMaxStages];
+    __shared__ int abort_s;
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kPipeMaxStages;
+    volatile int* abort_flag = &abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t qbytes = (uint32_t)a.hq * kD * kE, kbytes = (uint32_t)a.hkv * kD * kE;
+    if (tid < 5) sector[tid] = a.sector[tid];
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 33);  // the producer lane's expect-tx arrival + 32 lanes after the header/twiddles
+            mbar_init(&empty[s], kPipeConsumers);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kPipeConsumers) {
+        // ================================ producer ================================
+        const uint64_t policy = l2_evict_first_policy();
+        int n = 0;  // tokens started by this CTA
+        for (int t = blockIdx.x; t < a.num_tokens; t += gridDim.x, ++n) {
+            const int s = n % stages, use = n / stages;
+            unsigned char* st = smem + (size_t)s * stage_bytes;
+            bool go = true;
+            if (lane == 0) {
+                go = !*abort_flag;
+                if (go && use > 0) go = mbar_wait(&empty[s], (use - 1) & 1, a.status);
+                if (!go) {
+                    *abort_flag = 1;
+                } else {
+                    unsigned char* dq = st + 16 + kTwBytes;
+                    mbar_arrive_expect_tx(&full[s], qbytes + 2 * kbytes);
+                    bulk_load(dq, (const char*)a.q + (int64_t)t * qbytes, qbytes, &full[s], policy);
+                    bulk_load(dq + qbytes, (const char*)a.k + (int64_t)t * kbytes, kbytes, &full[s], policy);
+                    bulk_load(dq + qbytes + kbytes, (const char*)a.v + (int64_t)t * kbytes, kbytes, &full[s], policy);
+                }
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) break;
+            // the token's cache slot (the same for every lane)
+            const int pos = a.positions[t];
+            const int seq = a.seq_ids[t];
+            bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
+            long long blk = -1;
+            if (ok) {
+                blk = a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size];
+                ok = blk >= 0 && blk < a.num_blocks;
+            }
+            if (lane == 0) {
+                if (!ok) record_error(a.status, KVATTN_ERR_BAD_INDEX);
+                PipeHeader* h = reinterpret_cast<PipeHeader*>(st);
+                h->blk = ok ? blk : -1;
+                h->off = ok ? pos % a.block_size : 0;
+            }
+            if (ok) {
+                float4* tw = reinterpret_cast<float4*>(st + 16);
+                for (int i = lane; i < kPairs; i += 32) {
+                    ff c, sn;
+                    accurate_twiddle((uint64_t)(uint32_t)pos * a.turns[i], sector, c, sn);
+                    tw[i] = make_float4(c.hi, c.lo, sn.hi, sn.lo);
+                }
+            }
+            mbar_arrive(&full[s]);  // this lane's header/twiddle writes precede the arrival
+        }
+        // after an abort, let every armed copy land before the CTA can exit
+        if (lane == 0 && *abort_flag) {
+            const int m = n < stages ? n : stages;
+            for (int p = n - m; p < n; ++p) mbar_wait(&full[p % stages], (p / stages) & 1, a.status);
+        }
+        return;
+    }
+
+    // ================================ consumers ================================
+    // thread: column slice dv (fixed), heads hg, hg + kGroups, ... of q, k, v
+    const int dv = tid % kVPH, hg = tid / kVPH;
+    const int nq = max(0, (a.hq - hg + kGroups - 1) / kGroups);   // q heads of this thread
+    const int nk = max(0, (a.hkv - hg + kGroups - 1) / kGroups);  // k (and v) heads of this thread
+    const int nv = nq + 2 * nk;
+    int n = 0;
+    for (int t = blockIdx.x; t < a.num_tokens; t += gridDim.x, ++n) {
+        const int s = n % stages, use = n / stages;
+        const unsigned char* st = smem + (size_t)s * stage_bytes;
+        bool ready = !*abort_flag;
+        if (ready) ready = mbar_wait(&full[s], use & 1, a.status);
+        ready = __all_sync(0xffffffffu, ready);
+        if (!ready) {
+            if (lane == 0) *abort_flag = 1;
+            break;
+        }
+        const PipeHeader h = *reinterpret_cast<const PipeHeader*>(st);
+        if (h.blk >= 0) {
+            Twiddle2 tws[kPPV];
+#pragma unroll
+            for (int p = 0; p < kPPV; ++p) tws[p] = make_twiddle2(reinterpret_cast<const float4*>(st + 16) + dv * kPPV + p);
+            const unsigned char* src = st + 16 + kTwBytes;
+            for (int i = 0; i < nv; ++i) {
+                int64_t soff;  // byte offset of the vector inside the stage's rows
+                char* dst;
+                bool rot = true;
+                if (i < nq) {
+                    const int head = hg + i * kGroups;
+                    soff = ((int64_t)head * kD + dv * kEPV) * kE;
+                    dst = (char*)a.q + (int64_t)t * qbytes + soff;
+                } else {
+                    int u = i - nq;
+                    const bool isv = u >= nk;
+                    if (isv) u -= nk;
+                    rot = !isv;
+                    const int head = hg + u * kGroups;
+                    soff = (int64_t)qbytes + (isv ? kbytes : 0) + ((int64_t)head * kD + dv * kEPV) * kE;
+                    void* pool = isv ? a.v_pool : a.k_pool;
+                    dst = (char*)pool + ((((int64_t)h.blk * a.hkv + head) * a.block_size + h.off) * kD + dv * kEPV) * kE;
+                }
+                uint4 x = *reinterpret_cast<const uint4*>(src + soff);
+                if (rot) {
+                    if constexpr (kBF16) {
+                        x.x = rotate_bf16_word(x.x, tws[0]);
+                        x.y = rotate_bf16_word(x.y, tws[1]);
+                        x.z = rotate_bf16_word(x.z, tws[2]);
+                        x.w = rotate_bf16_word(x.w, tws[3]);
+                    } else {
+                        ff z0, z1, z2, z3;
+                        rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), *tws[0].ff, z0, z1);
+                        rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), *tws[1].ff, z2, z3);
+                        x = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
+                                       __float_as_uint(z3.hi));
+                    }
+                }
+                *reinterpret_cast<uint4*>(dst) = x;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+}  // namespace
+
+namespace {
+
+// Pipelined launch: stages of one token each (up to 4, within 64 KB per CTA),
+// as many persistent CTAs as fit on the GPU, at most one per token.  Returns
+// false (nothing launched) when a token's stage is too large for 2 stages.
+template <bool kBF16, int kD>
+bool launch_pipe(const RopeArgs& a, cudaStream_t s, cudaError_t& err)
+{
+    constexpr int kE = kBF16 ? 2 : 4;
+    const int64_t stage = 16 + (int64_t)(kD / 2) * 16 + (int64_t)(a.hq + 2 * a.hkv) * kD * kE;
+    const int stages = (int)std::min<int64_t>(4, 65536 / stage);
+    if (stages < 2) return false;
+    const int bytes = stages * (int)stage;
+    auto kern = rope_append_pipe_kernel<kBF16, kD>;
+    static std::mutex mu;
+    static int configured = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (bytes > configured) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (err != cudaSuccess) return true;
+            configured = bytes;
+        }
+    }
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, bytes);
+    if (err != cudaSuccess) return true;
+    const int grid = (int)std::min<int64_t>(a.num_tokens, (int64_t)num_sms() * std::max(1, per_sm));
+    kern<<<grid, kPipeThreads, bytes, s>>>(a, stages, (int)stage);
+    err = cudaGetLastError();
+    return true;
+}
+
+template <bool kBF16, int kD>
+kvattn_status launch_one(const RopeArgs& a, cudaStream_t s)
+{
+    cudaError_t err = cudaSuccess;
+    if (!launch_pipe<kBF16, kD>(a, s, err)) {
+        rope_append_kernel<kBF16, kD><<<a.num_tokens, 128, 0, s>>>(a);
+        err = cudaGetLastError();
+    }
+    return cuda_status(err);
+}
+
 }  // namespace
 
 kvattn_status launch_rope_append(const RopeArgs& a, cudaStream_t s)
 {
-    dim3 grid(a.num_tokens), block(128);
     const bool bf16 = a.dtype == KVATTN_BF16;
-    if (bf16 && a.d == 128) rope_append_kernel<true, 128><<<grid, block, 0, s>>>(a);
-    else if (bf16 && a.d == 64) rope_append_kernel<true, 64><<<grid, block, 0, s>>>(a);
-    else if (!bf16 && a.d == 128) rope_append_kernel<false, 128><<<grid, block, 0, s>>>(a);
-    else if (!bf16 && a.d == 64) rope_append_kernel<false, 64><<<grid, block, 0, s>>>(a);
-    else return KVATTN_ERR_UNSUPPORTED;
-    return cuda_status(cudaGetLastError());
+    if (bf16 && a.d == 128) return launch_one<true, 128>(a, s);
+    if (bf16 && a.d == 64) return launch_one<true, 64>(a, s);
+    if (!bf16 && a.d == 128) return launch_one<false, 128>(a, s);
+    if (!bf16 && a.d == 64) return launch_one<false, 64>(a, s);
+    return KVATTN_ERR_UNSUPPORTED;
 }
 
 }  // namespace kvattn
