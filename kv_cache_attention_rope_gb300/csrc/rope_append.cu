@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(kPipeThreads) rope_append_pipe_kernel(const __
     const int dv = tid % kVPH, hg = tid / kVPH;
     const int nq = max(0, (a.hq - hg + kGroups - 1) / kGroups);   // q heads of this thread
     const int nk = max(0, (a.hkv - hg + kGroups - 1) / kGroups);  // k (and v) heads of this thread
-    const int nv = nq + 2 * nk;
+    constexpr int kHeadStep = kGroups * kD * kE;             // bytes between this thread's heads in a row
+    const int slice = (hg * kD + dv * kEPV) * kE;             // byte offset of the first vector in a row
     int n = 0;
     for (int t = blockIdx.x; t < a.num_tokens; t += gridDim.x, ++n) {
         const int s = n % stages, use = n / stages;
@@ -445,41 +446,40 @@ __global__ void __launch_bounds__(kPipeThreads) rope_append_pipe_kernel(const __
             Twiddle2 tws[kPPV];
 #pragma unroll
             for (int p = 0; p < kPPV; ++p) tws[p] = make_twiddle2(reinterpret_cast<const float4*>(st + 16) + dv * kPPV + p);
-            const unsigned char* src = st + 16 + kTwBytes;
-            for (int i = 0; i < nv; ++i) {
-                int64_t soff;  // byte offset of the vector inside the stage's rows
-                char* dst;
-                bool rot = true;
-                if (i < nq) {
-                    const int head = hg + i * kGroups;
-                    soff = ((int64_t)head * kD + dv * kEPV) * kE;
-                    dst = (char*)a.q + (int64_t)t * qbytes + soff;
+            const unsigned char* src = st + 16 + kTwBytes + slice;  // this thread's column slice of head hg
+            auto rotate16 = [&](uint4 x) -> uint4 {
+                if constexpr (kBF16) {
+                    x.x = rotate_bf16_word(x.x, tws[0]);
+                    x.y = rotate_bf16_word(x.y, tws[1]);
+                    x.z = rotate_bf16_word(x.z, tws[2]);
+                    x.w = rotate_bf16_word(x.w, tws[3]);
                 } else {
-                    int u = i - nq;
-                    const bool isv = u >= nk;
-                    if (isv) u -= nk;
-                    rot = !isv;
-                    const int head = hg + u * kGroups;
-                    soff = (int64_t)qbytes + (isv ? kbytes : 0) + ((int64_t)head * kD + dv * kEPV) * kE;
-                    void* pool = isv ? a.v_pool : a.k_pool;
-                    dst = (char*)pool + ((((int64_t)h.blk * a.hkv + head) * a.block_size + h.off) * kD + dv * kEPV) * kE;
+                    ff z0, z1, z2, z3;
+                    rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), *tws[0].ff, z0, z1);
+                    rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), *tws[1].ff, z2, z3);
+                    x = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
+                                   __float_as_uint(z3.hi));
                 }
-                uint4 x = *reinterpret_cast<const uint4*>(src + soff);
-                if (rot) {
-                    if constexpr (kBF16) {
-                        x.x = rotate_bf16_word(x.x, tws[0]);
-                        x.y = rotate_bf16_word(x.y, tws[1]);
-                        x.z = rotate_bf16_word(x.z, tws[2]);
-                        x.w = rotate_bf16_word(x.w, tws[3]);
-                    } else {
-                        ff z0, z1, z2, z3;
-                        rotate_pair_ff(__uint_as_float(x.x), __uint_as_float(x.y), *tws[0].ff, z0, z1);
-                        rotate_pair_ff(__uint_as_float(x.z), __uint_as_float(x.w), *tws[1].ff, z2, z3);
-                        x = make_uint4(__float_as_uint(z0.hi), __float_as_uint(z1.hi), __float_as_uint(z2.hi),
-                                       __float_as_uint(z3.hi));
-                    }
-                }
-                *reinterpret_cast<uint4*>(dst) = x;
+                return x;
+            };
+            // q heads hg, hg + kGroups, ...: rotated in place
+            char* qdst = (char*)a.q + (int64_t)t * qbytes + slice;
+            for (int i = 0; i < nq; ++i) {
+                const uint4 x = *reinterpret_cast<const uint4*>(src + i * kHeadStep);
+                *reinterpret_cast<uint4*>(qdst + i * kHeadStep) = rotate16(x);
+            }
+            // k (rotated) and v (copied) heads into the token's cache slot
+            // pool layout [block][kv head][slot][D]: head hg's slot row, this thread's columns
+            const int64_t slot = (((int64_t)h.blk * a.hkv + hg) * a.block_size + h.off) * (kD * kE) + dv * kEPV * kE;
+            const int64_t pool_step = (int64_t)kGroups * a.block_size * (kD * kE);  // kGroups heads further
+            const unsigned char* ksrc = src + qbytes;
+            char* kdst = (char*)a.k_pool + slot;
+            char* vdst = (char*)a.v_pool + slot;
+            for (int u = 0; u < nk; ++u) {
+                const uint4 x = *reinterpret_cast<const uint4*>(ksrc + u * kHeadStep);
+                *reinterpret_cast<uint4*>(kdst + u * pool_step) = rotate16(x);
+                *reinterpret_cast<uint4*>(vdst + u * pool_step) =
+                    *reinterpret_cast<const uint4*>(ksrc + kbytes + u * kHeadStep);
             }
         }
         __syncwarp();

@@ -88,6 +88,19 @@ def test_rope_append_gqa8_block32(kvattn_lib):
     _run_case(kvattn_lib, "bf16", 16, 2, 128, 32, rows=5, maxb=40, T=150, max_pos=1280, seed=4)
 
 
+def test_rope_append_f32_gqa_d128_ring(kvattn_lib):
+    """fp32 q/k/v of 32/8 heads x 128 (24.6 KB per token): two ring stages per CTA."""
+    nq, nk, n = _run_case(kvattn_lib, "f32", 32, 8, 128, 16, rows=4, maxb=30, T=100, max_pos=480, seed=6)
+    assert nq + nk <= max(2, n * 1e-6)
+
+
+def test_rope_append_f32_many_heads_one_cta_per_token(kvattn_lib):
+    """fp32, 64 q heads x 128: a token (42 KB) does not fit two ring stages and
+    takes the one-CTA-per-token kernel."""
+    nq, nk, n = _run_case(kvattn_lib, "f32", 64, 8, 128, 16, rows=3, maxb=20, T=60, max_pos=320, seed=5)
+    assert nq + nk <= max(2, n * 1e-6)
+
+
 def test_rope_append_reports_bad_index_and_writes_the_rest(kvattn_lib):
     kv = kvattn_lib
     dev = torch.device("cuda")
