@@ -186,16 +186,12 @@ __device__ __noinline__ uint32_t rotate_bf16_word_slow(float x0, float x1, float
     return rne_bf16_ff(z0) | (rne_bf16_ff(z1) << 16);
 }
 
-// RNE to bf16 of y is also the RNE of every value within delta of y when the
-// fp32 pattern of y is more than delta away from a bf16 rounding boundary
-// (low 16 bits 0x8000).  Distance in fp32 ulps times |y| over-estimates the
-// distance times 2^23 by at most 2x, hence the conservative test
-// dist * |y| > 2^24 * delta.  Near-zero results fail it and take the slow path.
-__device__ __forceinline__ bool rounding_safe(float y, float delta_x_2p24)
-{
-    const int r = (int)(__float_as_uint(y) & 0xffffu) - 0x8000;
-    return fabsf((float)r) * fabsf(y) > delta_x_2p24;
-}
+// Rounding-safety test used below: RNE to bf16 of y is also the RNE of every
+// value within delta of y when the fp32 pattern of y is more than delta away
+// from a bf16 rounding boundary (low 16 bits 0x8000).  Distance in fp32 ulps
+// times |y| over-estimates the distance times 2^23 by at most 2x, hence the
+// conservative test dist * |y| > 2^24 * delta.  Near-zero results fail it and
+// take the slow path.
 
 // Rotates the bf16 pair packed in `w` (low half = even element).
 // Fast path: y = fl(fl(x0 (c, s)) + x1 (-s, c)) with the fp32-rounded
@@ -211,7 +207,15 @@ __device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const Twiddle2&
     const uint64_t y = ffma2(pk(x1, x1), tw.sc, fmul2(pk(x0, x0), tw.cs));
     const float y0 = pk_lo(y), y1 = pk_hi(y);
     const float dx = 8.0f * (fabsf(x0) + fabsf(x1));  // 2^24 * 2^-21 * (|x0| + |x1|)
-    if (rounding_safe(y0, dx) && rounding_safe(y1, dx)) return pack_bf16_rn(y0, y1);
+    // the rounding-safety test for both elements at once: the float with mantissa bits
+    // (low 16 bits of y) | 2^23, minus 2^23 + 2^15, is exactly
+    // (low 16 bits) - 0x8000, so no integer-to-float conversion is needed
+    constexpr float kBias = 8421376.0f;  // 2^23 + 2^15
+    const uint64_t r = fadd2(pk(__uint_as_float((__float_as_uint(y0) & 0xffffu) | 0x4b000000u),
+                                __uint_as_float((__float_as_uint(y1) & 0xffffu) | 0x4b000000u)),
+                             pk(-kBias, -kBias));
+    const uint64_t ry = fmul2(r, y);
+    if (fminf(fabsf(pk_lo(ry)), fabsf(pk_hi(ry))) > dx) return pack_bf16_rn(y0, y1);
     return rotate_bf16_word_slow(x0, x1, *tw.ff);
 }
 
