@@ -45,11 +45,12 @@ constexpr int kTile = 16;  // tokens per tile
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMinPer = 4;  // fewest tiles in a CTA's range (flat mode)
-// residency the register and shared-memory budgets aim at: 3 CTAs per SM on
-// the CUDA-core path; 2 on the tensor-core path, whose 16 x 8 accumulator
-// fragments need more registers and whose consumers need fewer warps
+// residency the register and shared-memory budgets aim at: 3 CTAs per SM
+// (the tensor-core path keeps only rows 0..7 of its 16 x 8 fragments, which
+// fits it in 128 registers; at 3 CTAs it reads c4 at the HBM copy rate, at 2
+// CTAs with more registers it reached 90%)
 template <bool kMma>
-constexpr int ctas_per_sm() { return kMma ? 2 : 3; }
+constexpr int ctas_per_sm() { return 3; }
 
 // Tensor maps of the K and V pools (tensor-core path).  Blocks of a multiple
 // of 16 tokens: one 4-D box per 16-token page, stage layout [8-row group]
@@ -425,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
                     qa[kk][1] = qrow[4 + q4];
                 }
             }
-            float o[kD / 8][4];
+            float o[kD / 8][2];  // rows 0..7 of each 16 x 8 output fragment (rows 8..15 are padding)
 #pragma unroll
-            for (int nd = 0; nd < kD / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+            for (int nd = 0; nd < kD / 8; ++nd) o[nd][0] = o[nd][1] = 0.f;
             float m_run = -INFINITY, lrun = 0.f;
             const float sl2 = a.scale_log2;
             for (int li = 0; li < ntiles; ++li) {
@@ -457,15 +458,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
                 }
                 // 16-byte chunk c of row r at chunk (c ^ r) of its 128 B (r = row mod 8)
                 const uint32_t kb = smem_addr(kst), vb = smem_addr(vst);
-                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-7, 8-15
+                float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};  // tokens 0-7, 8-15 (rows 0..7 of the fragments)
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     // matrices (tokens 0-7, chunk 2kk), (0-7, 2kk+1), (8-15, 2kk), (8-15, 2kk+1)
                     const int c = 2 * kk + (mi & 1), grp = mi >> 1;
                     uint32_t b[4];
                     ldmatrix_x4(b, kb + grp * gs + (c >> 3) * ps + rr * 128 + (((c & 7) ^ rr) << 4));
-                    mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b[0], b[1]);
-                    mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b[2], b[3]);
+                    mma_bf16_16816_top(s0, qa[kk][0], qa[kk][1], b[0], b[1]);
+                    mma_bf16_16816_top(s1, qa[kk][0], qa[kk][1], b[2], b[3]);
                 }
                 // row g4: tokens 2q4, 2q4+1 (s0) and 8+2q4, 9+2q4 (s1), in log2 units
                 float x[4] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2};
@@ -498,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
                     const int c = 2 * nd2 + (mi >> 1), grp = mi & 1;
                     uint32_t b[4];
                     ldmatrix_x4_trans(b, vb + grp * gs + (c >> 3) * ps + rr * 128 + (((c & 7) ^ rr) << 4));
-                    mma_bf16_16816(o[2 * nd2], pa0, 0u, pa2, 0u, b[0], b[1]);
-                    mma_bf16_16816(o[2 * nd2 + 1], pa0, 0u, pa2, 0u, b[2], b[3]);
+                    mma_bf16_16816_top(o[2 * nd2], pa0, pa2, b[0], b[1]);
+                    mma_bf16_16816_top(o[2 * nd2 + 1], pa0, pa2, b[2], b[3]);
                 }
                 if (nvalid < kTile) fence_async_smem();  // zeroed rows before the next copy into this stage
                 __syncwarp();

@@ -105,6 +105,19 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// As mma_bf16_16816 when rows 8..15 of A are zero: only rows 0..7 of the
+// accumulator (d0, d1) are kept; rows 8..15 start from zero and their results
+// go to scratch registers nothing reads, so they hold no registers across calls.
+__device__ __forceinline__ void mma_bf16_16816_top(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1)
+{
+    float z2, z3;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %10, %10};"
+        : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // ---- TMA (tensor maps) -----------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* m)
