@@ -116,6 +116,8 @@ __device__ __forceinline__ void mma_bf16_16816_top(float (&d)[2], uint32_t a0, u
         "{%0, %1, %10, %10};"
         : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    (void)z2;
+    (void)z3;
 }
 
 // ---- TMA (tensor maps) -----------------------------------------------------
