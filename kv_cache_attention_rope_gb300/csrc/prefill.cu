@@ -481,9 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ...): thread (quarter, lane) owns row r = 32 quarter + lane of the
         // tile, warps 2-5 its columns 0..63 (half hf = 0) and warps 6-9 its
         // columns 64..127 (hf = 1), so two warps per scheduler share each tile.
-        // The halves of a row agree on the row max through shared memory, one
-        // named barrier per tile; the barrier ANDs the waits' results, so a
-        // failed wait stops every softmax warp at the same point.
+        // The halves of a row (warps w and w + 4: the same TMEM lane quarter,
+        // the same scheduler) agree on the row max through shared memory, with
+        // a named barrier of that pair per tile; the barrier ANDs the pair's
+        // wait results, so a failed wait stops both halves at the same point
+        // (the other pairs stop at their next bounded wait).
         const int hf = (warp - 2) >> 2;
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;        // row of the tile
@@ -541,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     float* slot = xchg + ((2 * g + x) & 1) * 256;
                     slot[hf * 128 + r] = hm;
-                    if (!bar_and(1, 256, good)) {
+                    if (!bar_and(1 + quarter, 64, good)) {
                         ok = false;
                         break;
                     }
@@ -616,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* lx = xchg + 512;  // [2 halves][2 tiles][128 rows]
             lx[(hf * 2 + 0) * 128 + r] = lsum[0];
             lx[(hf * 2 + 1) * 128 + r] = lsum[1];
-            if (!bar_and(1, 256, good)) {
+            if (!bar_and(1 + quarter, 64, good)) {
                 ok = false;
                 break;
             }
