@@ -122,6 +122,39 @@ kvattn_status kvattn_rope_append(const kvattn_config* cfg, const kvattn_cache* c
                                  void* stream);
 
 /*
+ * kvattn_rope_append_strided -- kvattn_rope_append on row-strided q, k, v
+ * views, e.g. the three slices of one fused QKV projection output.
+ *
+ * [Series intro], section 5.1 (and the c_attn row of the weight table in
+ * section 5.2): one merged linear layer produces Q, K and V together,
+ * [seq_len][3 * hidden], and is then split; with grouped KV heads the row is
+ * [Hq*D | Hkv*D | Hkv*D].  Taking the three slices in place avoids copying
+ * them out before the rotation:
+ *     q = qkv,  k = qkv + Hq*D,  v = qkv + (Hq + Hkv)*D,
+ *     q_stride = k_stride = v_stride = (Hq + 2*Hkv)*D.
+ *
+ *   q_stride    elements from token t's q row to token t+1's (>= Hq*D)
+ *   k_stride    the same for k (>= Hkv*D)
+ *   v_stride    the same for v (>= Hkv*D)
+ *   q_out       device, dense [num_tokens][Hq][D], or NULL: where the rotated
+ *               q goes.  NULL rotates q in place (q stays read-write); a
+ *               buffer leaves the QKV output as it was and hands the
+ *               attention calls a dense q.
+ * Inside a row, heads and dimensions are contiguous ([H][D]).  Every row
+ * starts on a 16-byte boundary: the base pointers and stride * element size
+ * are multiples of 16 bytes.  The rows written (q in place, or q_out) must
+ * not overlap any row read by another token or any k or v row.  Everything
+ * else, results and errors, as kvattn_rope_append, which is this call with the
+ * dense strides Hq*D, Hkv*D, Hkv*D and q_out = NULL.  Errors in addition:
+ * INVALID_ARG for a stride below its row length or off the 16-byte rule.
+ */
+kvattn_status kvattn_rope_append_strided(const kvattn_config* cfg, const kvattn_cache* cache, void* q,
+                                         int64_t q_stride, const void* k, int64_t k_stride, const void* v,
+                                         int64_t v_stride, void* q_out, const int32_t* positions,
+                                         const int32_t* seq_ids, const int32_t* block_table, int32_t num_seqs,
+                                         int32_t max_blocks_per_seq, int32_t num_tokens, void* stream);
+
+/*
  * Workspace bytes kvattn_decode needs for `batch` sequences of at most
  * max_seq_len tokens with num_splits KV splits (0 = the library's choice for
  * the current device; the same arguments give the same choice).

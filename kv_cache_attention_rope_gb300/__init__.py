@@ -32,7 +32,8 @@ STATUS = {
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTED = [
-    "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_decode_workspace_size",
+    "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_rope_append_strided",
+    "kvattn_decode_workspace_size",
     "kvattn_decode_num_splits", "kvattn_decode", "kvattn_decode_static_scratch", "kvattn_prefill_chunk",
     "kvattn_selftest_wait_timeout", "kvattn_get_device_status",
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
@@ -70,6 +71,8 @@ def _load():
         "kvattn_version": ([], i32),
         "kvattn_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "kvattn_rope_append": ([cfgp, cachep, p, p, p, p, p, p, i32, i32, i32, p], ctypes.c_int),
+        "kvattn_rope_append_strided": ([cfgp, cachep, p, i64, p, i64, p, i64, p, p, p, p, i32, i32, i32, p],
+                                       ctypes.c_int),
         "kvattn_decode_workspace_size": ([cfgp, i32, i32, i32], sz),
         "kvattn_decode_num_splits": ([cfgp, i32, i32, i32], i32),
         "kvattn_decode": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p, sz, p], ctypes.c_int),
@@ -173,17 +176,74 @@ class Cache:
         return cls(k, v)
 
 
-def rope_append(cfg: Config, cache: Cache, q, k, v, positions, seq_ids, block_table, stream=None) -> None:
-    """kvattn_rope_append: rotate q in place, write rotated k and raw v into the cache."""
+def _rows(t, name: str, heads: int, head_dim: int, dtype=None):
+    """Pointer and row stride (elements) of a [T, heads, D] or [T, heads*D] view
+    whose rows are dense but may sit at any stride (a slice of a fused QKV row)."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    row = heads * head_dim
+    if t.dim() == 3 and tuple(t.shape[1:]) == (heads, head_dim):
+        dense = t.shape[2] <= 1 or t.stride(2) == 1
+        dense = dense and (t.shape[1] <= 1 or t.stride(1) == head_dim)
+    elif t.dim() == 2 and t.shape[1] == row:
+        dense = t.shape[1] <= 1 or t.stride(1) == 1
+    else:
+        raise ValueError(f"{name} must be [T, {heads}, {head_dim}] or [T, {row}]")
+    if not dense:
+        raise ValueError(f"{name}: each token's row must be dense (heads and dims contiguous)")
+    stride = t.stride(0) if t.shape[0] > 1 else row
+    return ctypes.c_void_p(t.data_ptr()), int(stride)
+
+
+def split_qkv(qkv, num_q_heads: int, num_kv_heads: int, head_dim: int):
+    """Views q [T,Hq,D], k [T,Hkv,D], v [T,Hkv,D] of one fused QKV projection
+    output [T, (Hq + 2 Hkv) D] (no copy); pass them to rope_append as they are."""
+    T = qkv.shape[0]
+    hq, hkv, d = num_q_heads, num_kv_heads, head_dim
+    if qkv.dim() != 2 or qkv.shape[1] != (hq + 2 * hkv) * d:
+        raise ValueError(f"qkv must be [T, {(hq + 2 * hkv) * d}]")
+    if qkv.stride(1) != 1:
+        raise ValueError("qkv rows must be dense")
+    q = qkv[:, : hq * d].view(T, hq, d)
+    k = qkv[:, hq * d: (hq + hkv) * d].view(T, hkv, d)
+    v = qkv[:, (hq + hkv) * d:].view(T, hkv, d)
+    return q, k, v
+
+
+def rope_append(cfg: Config, cache: Cache, q, k, v, positions, seq_ids, block_table, stream=None,
+                q_out=None) -> None:
+    """kvattn_rope_append: rotate q in place (or into q_out), write rotated k and
+    raw v into the cache.
+
+    q, k, v are dense [T, H, D] tensors, or row-strided views (split_qkv of a
+    fused QKV output); those, or a q_out, go through kvattn_rope_append_strided."""
     torch = _torch()
     T = q.shape[0]
-    check(lib.kvattn_rope_append(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q"),
-                                 _dev(k, "k", q.dtype), _dev(v, "v", q.dtype),
-                                 _dev(positions, "positions", torch.int32),
-                                 _dev(seq_ids, "seq_ids", torch.int32),
-                                 _dev(block_table, "block_table", torch.int32),
-                                 block_table.shape[0], block_table.shape[1], T, _stream(stream)),
-          "kvattn_rope_append")
+    hq, hkv, d = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+    common = (_dev(positions, "positions", torch.int32), _dev(seq_ids, "seq_ids", torch.int32),
+              _dev(block_table, "block_table", torch.int32),
+              block_table.shape[0], block_table.shape[1], T, _stream(stream))
+    if q_out is None and q.is_contiguous() and k.is_contiguous() and v.is_contiguous():
+        check(lib.kvattn_rope_append(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q"),
+                                     _dev(k, "k", q.dtype), _dev(v, "v", q.dtype), *common),
+              "kvattn_rope_append")
+        return
+    qp, qs = _rows(q, "q", hq, d)
+    kp, ks = _rows(k, "k", hkv, d, q.dtype)
+    vp, vs = _rows(v, "v", hkv, d, q.dtype)
+    qo = None
+    if q_out is not None:
+        if tuple(q_out.shape) != (T, hq, d):
+            raise ValueError(f"q_out must be [{T}, {hq}, {d}]")
+        qo = _dev(q_out, "q_out", q.dtype)
+    check(lib.kvattn_rope_append_strided(ctypes.byref(cfg), ctypes.byref(cache.desc), qp, qs, kp, ks, vp, vs,
+                                         qo, *common),
+          "kvattn_rope_append_strided")
 
 
 def decode_workspace_size(cfg: Config, batch: int, max_seq_len: int, num_splits: int = 0) -> int:

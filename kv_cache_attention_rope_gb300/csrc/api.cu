@@ -2,6 +2,7 @@
 // kernels.  Every check the host can make is made here, before any launch.
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 
@@ -163,19 +164,46 @@ kvattn_status kvattn_rope_append(const kvattn_config* cfg, const kvattn_cache* c
                                  const int32_t* block_table, int32_t num_seqs, int32_t max_blocks_per_seq,
                                  int32_t num_tokens, void* stream)
 {
+    if (!config_ok(cfg)) return KVATTN_ERR_INVALID_ARG;
+    const int64_t qrow = (int64_t)cfg->num_q_heads * cfg->head_dim;
+    const int64_t kvrow = (int64_t)cfg->num_kv_heads * cfg->head_dim;
+    return kvattn_rope_append_strided(cfg, cache, q, qrow, k, kvrow, v, kvrow, nullptr, positions, seq_ids,
+                                      block_table, num_seqs, max_blocks_per_seq, num_tokens, stream);
+}
+
+kvattn_status kvattn_rope_append_strided(const kvattn_config* cfg, const kvattn_cache* cache, void* q,
+                                         int64_t q_stride, const void* k, int64_t k_stride, const void* v,
+                                         int64_t v_stride, void* q_out, const int32_t* positions,
+                                         const int32_t* seq_ids, const int32_t* block_table, int32_t num_seqs,
+                                         int32_t max_blocks_per_seq, int32_t num_tokens, void* stream)
+{
     if (!config_ok(cfg) || num_tokens < 0 || num_seqs <= 0) return KVATTN_ERR_INVALID_ARG;
     kvattn_status st = config_supported(cfg);
     if (st != KVATTN_OK) return st;
     if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
+    // a row never overlaps the next one, and every row starts on a 16-byte boundary
+    const int64_t e = cfg->dtype == KVATTN_BF16 ? 2 : 4;
+    const int64_t qrow = (int64_t)cfg->num_q_heads * cfg->head_dim;
+    const int64_t kvrow = (int64_t)cfg->num_kv_heads * cfg->head_dim;
+    const int64_t max_stride = INT64_MAX / 4 / std::max<int64_t>(1, num_tokens);
+    if (q_stride < qrow || k_stride < kvrow || v_stride < kvrow) return KVATTN_ERR_INVALID_ARG;
+    if (q_stride > max_stride || k_stride > max_stride || v_stride > max_stride) return KVATTN_ERR_INVALID_ARG;
+    if (((q_stride | k_stride | v_stride) * e) & 15) return KVATTN_ERR_INVALID_ARG;
     if (num_tokens == 0) return KVATTN_OK;
     if (!q || !k || !v || !positions || !seq_ids || !block_table) return KVATTN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(q_out)) & 15u)
         return KVATTN_ERR_INVALID_ARG;
     RopeArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q = q;
     a.k = k;
     a.v = v;
+    a.q_stride = q_stride * e;
+    a.k_stride = k_stride * e;
+    a.v_stride = v_stride * e;
+    a.q_out = q_out ? q_out : q;
+    a.q_out_stride = q_out ? qrow * e : a.q_stride;
     a.k_pool = cache->k_pool;
     a.v_pool = cache->v_pool;
     a.positions = positions;

@@ -26,6 +26,9 @@ struct RopeArgs {
     void* q;
     const void* k;
     const void* v;
+    int64_t q_stride, k_stride, v_stride;  // bytes from one token's row to the next
+    void* q_out;                           // rotated q rows (== q: in place)
+    int64_t q_out_stride;                  // bytes
     void* k_pool;
     void* v_pool;
     const int32_t* positions;

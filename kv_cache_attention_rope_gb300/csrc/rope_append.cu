@@ -4,9 +4,12 @@
 // x[2i+1]) of a query/key head vector rotate by m*theta_i, theta_i =
 // base^(-2i/D), m = the token position.  "From-scratch AI inference engine"
 // page, section 3.2: the new token's K/V go to the cache index equal to that
-// same position.  Every q head is rotated in place, every k head rotated into
-// the cache slot and v copied into the cache slot, in 16-byte vectors (8 bf16
-// / 4 fp32 values).  Persistent CTAs stream the tokens through a shared-memory
+// same position.  Every q head is rotated (in place, or into a separate dense
+// q buffer), every k head rotated into the cache slot and v copied into the
+// cache slot, in 16-byte vectors (8 bf16 / 4 fp32 values).  q, k and v are
+// rows at any 16-byte-multiple stride, so they can be the three slices of one
+// fused QKV projection output ("hand-written LLM inference engine" series,
+// chapter 1, section 5.1: GPT-2's merged c_attn layer).  Persistent CTAs stream the tokens through a shared-memory
 // ring (rope_append_pipe_kernel); a token too large for two ring stages takes
 // the one-CTA-per-token kernel (rope_append_kernel).
 //
@@ -239,11 +242,12 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
     const int nk = (a.hkv - hg + kGroups - 1) / kGroups;  // k (and v) heads of this thread
     const int nv = max(0, nq) + 2 * max(0, nk);
     auto src_of = [&](int i) -> const char* {  // i-th vector of this thread
-        if (i < nq) return (const char*)a.q + (((int64_t)t * a.hq + hg + i * kGroups) * kD + dv * kEPV) * kE;
+        if (i < nq) return (const char*)a.q + t * a.q_stride + ((hg + i * kGroups) * kD + dv * kEPV) * kE;
         i -= nq;
-        const char* base = (const char*)(i < nk ? a.k : a.v);
-        if (i >= nk) i -= nk;
-        return base + (((int64_t)t * a.hkv + hg + i * kGroups) * kD + dv * kEPV) * kE;
+        const bool isv = i >= nk;
+        const char* row = isv ? (const char*)a.v + t * a.v_stride : (const char*)a.k + t * a.k_stride;
+        if (isv) i -= nk;
+        return row + ((hg + i * kGroups) * kD + dv * kEPV) * kE;
     };
 
     // first loads: independent of the position lookups below
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
             char* dst;
             bool rot = true;
             if (i < nq) {
-                dst = const_cast<char*>(src_of(i));
+                dst = (char*)a.q_out + t * a.q_out_stride + ((hg + i * kGroups) * kD + dv * kEPV) * kE;
             } else {
                 int u = i - nq;
                 const bool isv = u >= nk;
@@ -326,8 +330,8 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
 // Warp 4 is the producer: per token one lane starts 1-D bulk copies of the
 // token's q, k and v rows into a ring stage, and while they fly the warp looks
 // up the token's cache slot and computes its float-float twiddles into the
-// same stage.  Warps 0-3 rotate from shared memory and write q back in place
-// and k, v to the cache slot.  A token's loads no longer wait for the previous
+// same stage.  Warps 0-3 rotate from shared memory and write q out (in place
+// or to q_out) and k, v to the cache slot.  A token's loads no longer wait for the previous
 // token's compute, so a CTA keeps several tokens' bytes in flight.
 // Stage layout: [header 16 B][twiddles, kPairs x 16 B][q row][k row][v row].
 constexpr int kPipeConsumers = 4;
@@ -387,9 +391,9 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
                 } else {
                     unsigned char* dq = st + 16 + kTwBytes;
                     mbar_arrive_expect_tx(&full[s], qbytes + 2 * kbytes);
-                    bulk_load(dq, (const char*)a.q + (int64_t)t * qbytes, qbytes, &full[s], policy);
-                    bulk_load(dq + qbytes, (const char*)a.k + (int64_t)t * kbytes, kbytes, &full[s], policy);
-                    bulk_load(dq + qbytes + kbytes, (const char*)a.v + (int64_t)t * kbytes, kbytes, &full[s], policy);
+                    bulk_load(dq, (const char*)a.q + t * a.q_stride, qbytes, &full[s], policy);
+                    bulk_load(dq + qbytes, (const char*)a.k + t * a.k_stride, kbytes, &full[s], policy);
+                    bulk_load(dq + qbytes + kbytes, (const char*)a.v + t * a.v_stride, kbytes, &full[s], policy);
                 }
             }
             go = __shfl_sync(0xffffffffu, go, 0);
@@ -466,8 +470,8 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
                 }
                 return x;
             };
-            // q heads hg, hg + kGroups, ...: rotated in place
-            char* qdst = (char*)a.q + (int64_t)t * qbytes + slice;
+            // q heads hg, hg + kGroups, ...: rotated into q_out (in place when q_out == q)
+            char* qdst = (char*)a.q_out + t * a.q_out_stride + slice;
             for (int i = 0; i < nq; ++i) {
                 const uint4 x = *reinterpret_cast<const uint4*>(src + i * kHeadStep);
                 *reinterpret_cast<uint4*>(qdst + i * kHeadStep) = rotate16(x);

@@ -15,7 +15,8 @@ from _gpu_support import OR_DT, TORCH_DT, check_rotation, f64, get_rows
 pytestmark = pytest.mark.gpu
 
 
-def _run_case(kv, dtype, Hq, Hkv, D, BS, rows, maxb, T, max_pos, seed, contiguous=False):
+def _run_case(kv, dtype, Hq, Hkv, D, BS, rows, maxb, T, max_pos, seed, contiguous=False, fused_pad=None,
+              separate_q_out=False):
     dev = torch.device("cuda")
     g = np.random.default_rng(seed)
     dt = TORCH_DT[dtype]
@@ -43,10 +44,30 @@ def _run_case(kv, dtype, Hq, Hkv, D, BS, rows, maxb, T, max_pos, seed, contiguou
     cache = kv.Cache.empty(nb, Hkv, BS, D, dt, dev)
     cache.k_pool.fill_(float("nan"))
     cache.v_pool.fill_(float("nan"))
-    qd = q.to(dev)
-    kv.rope_append(cfg, cache, qd, k.to(dev), v.to(dev), torch.from_numpy(pos).to(dev),
-                   torch.from_numpy(seq).to(dev), torch.from_numpy(table).to(dev))
+    if fused_pad is None:
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    else:
+        # one fused QKV projection output per token, [q | k | v | pad], taken as strided views
+        width = (Hq + 2 * Hkv) * D
+        buf = torch.full((T, width + fused_pad), -7.0, dtype=dt, device=dev)
+        buf[:, :width] = torch.cat([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], 1).to(dev)
+        qd, kd, vd = kv.split_qkv(buf[:, :width], Hq, Hkv, D)
+        assert not qd.is_contiguous()
+    q_out = torch.full((T, Hq, D), float("nan"), dtype=dt, device=dev) if separate_q_out else None
+    kv.rope_append(cfg, cache, qd, kd, vd, torch.from_numpy(pos).to(dev),
+                   torch.from_numpy(seq).to(dev), torch.from_numpy(table).to(dev), q_out=q_out)
     assert kv.get_device_status() == 0
+    bits = torch.int16 if dtype == "bf16" else torch.int32
+    if fused_pad is not None:
+        # only the q slices were written (none of the buffer with a separate q_out)
+        hb = buf.cpu()
+        first = Hq * D if q_out is None else 0
+        kept = torch.cat([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], 1)[:, first:]
+        assert torch.equal(hb[:, first: width].view(bits), kept.view(bits))
+        assert bool((hb[:, width:] == -7.0).all())
+    if q_out is not None:
+        assert torch.equal(qd.cpu().view(bits), q.view(bits))  # the input q is left as it was
+        qd = q_out
     # q in place
     q_exact = oracle.rope(q.double().numpy(), pos)
     nq = check_rotation(f64(qd), q_exact, dtype, "q")
@@ -98,6 +119,41 @@ def test_rope_append_f32_many_heads_one_cta_per_token(kvattn_lib):
     """fp32, 64 q heads x 128: a token (42 KB) does not fit two ring stages and
     takes the one-CTA-per-token kernel."""
     nq, nk, n = _run_case(kvattn_lib, "f32", 64, 8, 128, 16, rows=3, maxb=20, T=60, max_pos=320, seed=5)
+    assert nq + nk <= max(2, n * 1e-6)
+
+
+def test_rope_append_fused_qkv_bf16_gqa(kvattn_lib):
+    """q, k, v as slices of one fused [T, (32 + 2*8) * 128] projection output."""
+    nq, nk, n = _run_case(kvattn_lib, "bf16", 32, 8, 128, 16, rows=6, maxb=200, T=300, max_pos=3200, seed=7,
+                          fused_pad=0)
+    assert nq + nk <= max(2, n * 1e-6), (nq, nk)
+
+
+def test_rope_append_fused_qkv_padded_rows_f32_gpt2_shape(kvattn_lib):
+    """GPT-2 12 x 64 heads in fp32, fused rows padded by 8 elements (row stride 2312)."""
+    nq, nk, n = _run_case(kvattn_lib, "f32", 12, 12, 64, 128, rows=2, maxb=1, T=200, max_pos=128, seed=8,
+                          contiguous=True, fused_pad=8)
+    assert nq + nk <= max(2, n * 1e-6)
+
+
+def test_rope_append_fused_qkv_separate_q_out(kvattn_lib):
+    """Fused QKV rows left untouched, rotated q written to a dense q_out (ring kernel)."""
+    nq, nk, n = _run_case(kvattn_lib, "bf16", 32, 8, 128, 16, rows=4, maxb=100, T=200, max_pos=1600, seed=10,
+                          fused_pad=16, separate_q_out=True)
+    assert nq + nk <= max(2, n * 1e-6), (nq, nk)
+
+
+def test_rope_append_separate_q_out_one_cta_per_token(kvattn_lib):
+    """Dense inputs with a separate q_out, fp32 64/8 x 128: the one-CTA-per-token kernel."""
+    nq, nk, n = _run_case(kvattn_lib, "f32", 64, 8, 128, 16, rows=3, maxb=20, T=40, max_pos=320, seed=11,
+                          separate_q_out=True)
+    assert nq + nk <= max(2, n * 1e-6)
+
+
+def test_rope_append_fused_qkv_one_cta_per_token(kvattn_lib):
+    """fp32 64/8 x 128 (too large for two ring stages): the one-CTA-per-token kernel on strided rows."""
+    nq, nk, n = _run_case(kvattn_lib, "f32", 64, 8, 128, 16, rows=3, maxb=20, T=60, max_pos=320, seed=9,
+                          fused_pad=4)
     assert nq + nk <= max(2, n * 1e-6)
 
 

@@ -80,6 +80,56 @@ def test_rope_append_validation(kv):
     assert _rope(kv, good, _cache(kv), q=None) == E["KVATTN_ERR_INVALID_ARG"]
 
 
+def _rope_strided(kv, cfg, cache, qs, ks, vs, T=4, q=FAKE, q_out=None):
+    return kv.lib.kvattn_rope_append_strided(ctypes.byref(cfg), ctypes.byref(cache), q, qs, FAKE, ks, FAKE, vs,
+                                             q_out, FAKE, FAKE, FAKE, 1, 1, T, None)
+
+
+def test_rope_append_strided_validation(kv):
+    E = kv.STATUS_CODE
+    cfg = kv.make_config(8, 2, 128, kv.BF16)
+    fused = (8 + 2 * 2) * 128
+    c = _cache(kv)
+    # the fused-QKV strides and the dense strides pass host validation (T = 0 launches nothing)
+    assert _rope_strided(kv, cfg, c, fused, fused, fused, T=0) == E["KVATTN_OK"]
+    assert _rope_strided(kv, cfg, c, 8 * 128, 2 * 128, 2 * 128, T=0) == E["KVATTN_OK"]
+    # a stride below its row length would overlap rows
+    assert _rope_strided(kv, cfg, c, 8 * 128 - 8, fused, fused, T=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope_strided(kv, cfg, c, fused, 2 * 128 - 8, fused, T=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope_strided(kv, cfg, c, fused, fused, 1, T=0) == E["KVATTN_ERR_INVALID_ARG"]
+    # rows must start on 16-byte boundaries: bf16 strides in multiples of 8, f32 in multiples of 4
+    assert _rope_strided(kv, cfg, c, fused + 4, fused, fused, T=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope_strided(kv, cfg, c, fused, fused, fused + 8, T=0) == E["KVATTN_OK"]
+    f32 = kv.make_config(8, 2, 128, kv.F32)
+    assert _rope_strided(kv, f32, c, fused + 4, fused, fused, T=0) == E["KVATTN_OK"]
+    assert _rope_strided(kv, f32, c, fused + 2, fused, fused, T=0) == E["KVATTN_ERR_INVALID_ARG"]
+    # strides whose byte offsets would overflow
+    assert _rope_strided(kv, cfg, c, 2 ** 62, fused, fused) == E["KVATTN_ERR_INVALID_ARG"]
+    # misaligned base pointer, null q
+    assert _rope_strided(kv, cfg, c, fused, fused, fused, q=ctypes.c_void_p(0x7F0000001008)) == \
+        E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope_strided(kv, cfg, c, fused, fused, fused, q=None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert _rope_strided(kv, cfg, c, fused, fused, fused, q_out=ctypes.c_void_p(0x7F0000002004)) == \
+        E["KVATTN_ERR_INVALID_ARG"]
+
+
+def test_split_qkv_views(kv):
+    import torch
+
+    T, hq, hkv, d = 5, 8, 2, 64
+    qkv = torch.arange(T * (hq + 2 * hkv) * d, dtype=torch.float32).view(T, -1)
+    q, k, v = kv.split_qkv(qkv, hq, hkv, d)
+    assert q.shape == (T, hq, d) and k.shape == (T, hkv, d) and v.shape == (T, hkv, d)
+    row = (hq + 2 * hkv) * d
+    assert q.stride() == k.stride() == v.stride() == (row, d, 1)
+    assert k.data_ptr() - q.data_ptr() == hq * d * 4
+    assert v.data_ptr() - k.data_ptr() == hkv * d * 4
+    # the views alias the fused buffer (no copy)
+    assert torch.equal(torch.cat([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], 1), qkv)
+    with pytest.raises(ValueError):
+        kv.split_qkv(qkv[:, :-d], hq, hkv, d)
+
+
 def _decode(kv, cfg, cache, B=2, maxlen=64, splits=0, ws=None, ws_bytes=0, out=FAKE, maxb=4):
     return kv.lib.kvattn_decode(ctypes.byref(cfg), ctypes.byref(cache), FAKE, FAKE, maxb, FAKE, B, maxlen,
                                 splits, out, ws, ws_bytes, None)
