@@ -50,6 +50,9 @@ def parse_args():
                    help="use only the first N prefill chunks of the workload (profiling small cases)")
     p.add_argument("--compact-pool", action="store_true",
                    help="pool of twice the blocks the batch needs instead of the workload's pool size")
+    p.add_argument("--layers", type=int, default=1,
+                   help="run the step over L layers: one multi-layer cache, each layer's q/k/v taken as views "
+                        "of its own fused QKV projection output, rotated q into a dense buffer")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -169,12 +172,14 @@ class ClockSampler:
 class Step:
     """A workload's step on one GPU, inputs resident in HBM."""
 
-    def __init__(self, wl: workloads.Workload, device, rows: int = 0, compact_pool: bool = False, chunks: int = -1):
+    def __init__(self, wl: workloads.Workload, device, rows: int = 0, compact_pool: bool = False, chunks: int = -1,
+                 layers: int = 1):
         import torch
 
         import kv_cache_attention_rope_gb300 as kv
 
         self.kv, self.torch, self.wl, self.dev = kv, torch, wl, device
+        self.layers = max(1, int(layers))
         dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
         self.dt = dt
         H, D, BS = wl.num_kv_heads, wl.head_dim, wl.block_size
@@ -194,18 +199,24 @@ class Step:
                 nb = int(2 * ((probe.total + BS - 1) // BS).sum())
             elif wl.pool_bytes:
                 nb = wl.pool_bytes // per_block
+        self.cfg = kv.make_config(wl.num_q_heads, H, D, kv.BF16 if wl.dtype == "bf16" else kv.F32)
         # batch (prefill chunks first, then decode rows); shrink a huge pool until it fits
         while True:
             batch = workloads.make_batch(wl, num_blocks=nb, rows_subset=subset)
             try:
-                cache = kv.Cache.empty(batch.num_blocks, H, BS, D, dt, device)
+                if self.layers == 1:
+                    self.caches = [kv.Cache.empty(batch.num_blocks, H, BS, D, dt, device)]
+                else:
+                    # one block id names 2 x layers regions of one allocation
+                    self.layered = kv.LayeredCache.empty(self.cfg, self.layers, batch.num_blocks, BS, dt, device)
+                    self.caches = [self.layered.layer(l) for l in range(self.layers)]
                 break
             except torch.OutOfMemoryError:
                 nb = batch.num_blocks // 2
                 torch.cuda.empty_cache()
+        cache = self.caches[0]
         self.batch, self.cache = batch, cache
-        self.pool_bytes = batch.num_blocks * per_block
-        self.cfg = kv.make_config(wl.num_q_heads, H, D, kv.BF16 if wl.dtype == "bf16" else kv.F32)
+        self.pool_bytes = batch.num_blocks * per_block * self.layers
         nchunk = wl.chunks
         self.nchunk = nchunk
         past, new = batch.past, batch.new
@@ -238,12 +249,13 @@ class Step:
         blk = self.table_host[rows, pos // BS].astype(np.int64)
         off = (pos % BS).astype(np.int64)
         step = 1 << 17
-        for s in range(0, len(pos), step):
-            b = torch.from_numpy(blk[s:s + step]).to(device)
-            o = torch.from_numpy(off[s:s + step]).to(device)
-            n = len(b)
-            cache.k_pool[b, :, o, :] = torch.randn((n, H, D), generator=gen, device=device).to(dt)
-            cache.v_pool[b, :, o, :] = torch.randn((n, H, D), generator=gen, device=device).to(dt)
+        for c in self.caches:
+            for s in range(0, len(pos), step):
+                b = torch.from_numpy(blk[s:s + step]).to(device)
+                o = torch.from_numpy(off[s:s + step]).to(device)
+                n = len(b)
+                c.k_pool[b, :, o, :] = torch.randn((n, H, D), generator=gen, device=device).to(dt)
+                c.v_pool[b, :, o, :] = torch.randn((n, H, D), generator=gen, device=device).to(dt)
         # ---- this step's new tokens (prefill chunk tokens, then one per decode row)
         q_l, k_l, v_l, p_l, s_l = [], [], [], [], []
         for r in range(batch.rows):
@@ -266,6 +278,17 @@ class Step:
         self.q = self.h_q.to(device)
         self.k = self.h_k.to(device)
         self.v = self.h_v.to(device)
+        self.views = []
+        if self.layers > 1:
+            # each layer's fused QKV projection output [T, (Hq + 2 Hkv) D]: layer 0 holds this
+            # step's tokens, the others fresh N(0,1) rows; q is rotated into the dense self.q
+            T = self.h_q.shape[0]
+            for l in range(self.layers):
+                if l == 0:
+                    x = torch.cat([self.q.reshape(T, -1), self.k.reshape(T, -1), self.v.reshape(T, -1)], 1)
+                else:
+                    x = torch.randn((T, (wl.num_q_heads + 2 * H) * D), generator=gen, device=device).to(dt)
+                self.views.append(kv.split_qkv(x, wl.num_q_heads, H, D))
         self.pos = self.h_pos.to(device)
         self.sid = self.h_sid.to(device)
         self.lens = self.h_lens.to(device)
@@ -289,15 +312,17 @@ class Step:
         self.h_out_pre = torch.empty(self.out_pre.shape, dtype=dt).pin_memory()
         # algorithmic bytes / flops
         E = wl.elem_bytes
-        self.kv_bytes_decode = workloads.kv_bytes_read(wl, total[nchunk:])
-        self.kv_bytes_prefill = workloads.kv_bytes_read(wl, total[:nchunk])
-        self.rope_bytes = self.n_tok * 2 * (wl.num_q_heads + 2 * H) * D * E
+        Lr = self.layers
+        self.kv_bytes_decode = Lr * workloads.kv_bytes_read(wl, total[nchunk:])
+        self.kv_bytes_prefill = Lr * workloads.kv_bytes_read(wl, total[:nchunk])
+        self.rope_bytes = Lr * self.n_tok * 2 * (wl.num_q_heads + 2 * H) * D * E
         pre_flops = 0
         for c in range(nchunk):
             P, n = int(past[c]), int(new[c])
             pre_flops += 4 * D * wl.num_q_heads * int(np.sum(P + np.arange(n) + 1))
-        self.prefill_flops = pre_flops
-        self.launches_per_step = 1 + (1 if self.n_dec else 0) + (1 if self.splits > 1 else 0) + (1 if nchunk else 0)
+        self.prefill_flops = Lr * pre_flops
+        self.launches_per_step = Lr * (1 + (1 if self.n_dec else 0) + (1 if self.splits > 1 else 0) +
+                                       (1 if nchunk else 0))
 
     # host block allocator: hand out the blocks this step's tokens open, return them after
     def alloc_begin(self):
@@ -312,23 +337,31 @@ class Step:
             self.alloc.free(ids[::-1])
 
     def launch(self, ev=None):
+        """One step: per layer rope_append, prefill_chunk, decode.  ev: per layer
+        four events bracketing the three kernels."""
         kv = self.kv
         ids = self.alloc_begin()
-        if ev is not None:
-            ev[0].record()
-        kv.rope_append(self.cfg, self.cache, self.q, self.k, self.v, self.pos, self.sid, self.d_table)
-        if ev is not None:
-            ev[1].record()
-        if self.nchunk:
-            kv.prefill_chunk(self.cfg, self.cache, self.q_pre, self.cu, self.prefix, self.d_table_pre, self.max_q,
-                             out=self.out_pre)
-        if ev is not None:
-            ev[2].record()
-        if self.n_dec:
-            kv.decode(self.cfg, self.cache, self.q_dec, self.d_table_dec, self.lens, self.max_len, out=self.out_dec,
-                      workspace=self.ws)
-        if ev is not None:
-            ev[3].record()
+        for l, cache in enumerate(self.caches):
+            e = ev[l] if ev is not None else None
+            if e is not None:
+                e[0].record()
+            if self.views:
+                q, k, v = self.views[l]
+                kv.rope_append(self.cfg, cache, q, k, v, self.pos, self.sid, self.d_table, q_out=self.q)
+            else:
+                kv.rope_append(self.cfg, cache, self.q, self.k, self.v, self.pos, self.sid, self.d_table)
+            if e is not None:
+                e[1].record()
+            if self.nchunk:
+                kv.prefill_chunk(self.cfg, cache, self.q_pre, self.cu, self.prefix, self.d_table_pre, self.max_q,
+                                 out=self.out_pre)
+            if e is not None:
+                e[2].record()
+            if self.n_dec:
+                kv.decode(self.cfg, cache, self.q_dec, self.d_table_dec, self.lens, self.max_len,
+                          out=self.out_dec, workspace=self.ws)
+            if e is not None:
+                e[3].record()
         self.alloc_end(ids)
 
     def _host_inputs(self, b=0):
@@ -469,7 +502,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     wl = workloads.WORKLOADS[args.workload]
-    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool, chunks=args.chunks)
+    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool, chunks=args.chunks, layers=args.layers)
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
@@ -479,7 +512,7 @@ def run_ours(args, rank, world):
     if status:
         raise RuntimeError(f"device status {st.kv.STATUS.get(status)} after warm-up")
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(st.layers)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev)
     if world > 1:
@@ -495,23 +528,24 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     elapsed = start.elapsed_time(end) / 1e3
-    t_rope = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
-    t_pre = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
-    t_dec = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 1e3
+    # per step: summed over the step's layers
+    t_rope = statistics.mean(sum(e[0].elapsed_time(e[1]) for e in es) for es in evs) / 1e3
+    t_pre = statistics.mean(sum(e[1].elapsed_time(e[2]) for e in es) for es in evs) / 1e3
+    t_dec = statistics.mean(sum(e[2].elapsed_time(e[3]) for e in es) for es in evs) / 1e3
     status = st.kv.get_device_status()
     if status:
         raise RuntimeError(f"device status {st.kv.STATUS.get(status)} in the timed region")
     # e2e through host buffers
     e2e = None
     e2e_t = 0.0
-    if not args.no_e2e:
+    if not args.no_e2e and st.layers == 1:
         st.e2e_setup()
         st.run_e2e(3)  # warm-up
         e2e_t = st.run_e2e(K)
     elapsed, e2e_t = max_over_ranks([elapsed, e2e_t], dev)
     step_bytes = st.kv_bytes_decode + st.kv_bytes_prefill
     value = whole_job_rate(step_bytes, K, world, elapsed) / 1e9
-    if not args.no_e2e:
+    if not args.no_e2e and st.layers == 1:
         e2e = {"value": whole_job_rate(step_bytes, K, world, e2e_t) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": st.h2d_bytes(),
                "d2h_bytes_per_step": st.d2h_bytes(), "ms_per_step": 1e3 * e2e_t / K}
@@ -544,7 +578,11 @@ def run_ours(args, rank, world):
                    "kv_bytes_per_step": step_bytes, "decode_splits": st.splits,
                    "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of KV per step)"
                    if step_bytes > 2e8 else "L2-resident: KV smaller than L2, not flushed",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "layers": st.layers,
+                   **({"qkv_input": "per layer: views of its fused [T, (Hq+2Hkv)D] QKV output; q rotated into "
+                                    "a dense buffer; no host upload (e2e measured at layers=1)"}
+                      if st.layers > 1 else {})},
         "query_tokens_per_s": whole_job_rate(st.n_tok, K, world, elapsed),
         "hbm_frac": (st.kv_bytes_decode / t_dec / 1e9) / hbm if st.n_dec else None,
         "kernels_ms": {k: 1e3 * v for k, v in parts.items()},

@@ -155,6 +155,32 @@ kvattn_status kvattn_rope_append_strided(const kvattn_config* cfg, const kvattn_
                                          int32_t max_blocks_per_seq, int32_t num_tokens, void* stream);
 
 /*
+ * Multi-layer cache: one device allocation holding every layer's K area and V
+ * area, so that one block id (one block-table entry, one allocator) names the
+ * same block in all of them.
+ *
+ * [Nano-vLLM], section 05 (5.2): each decoder layer keeps its own K cache
+ * area and V cache area, so a logical block index maps to L x 2 physical
+ * regions (48 for a 24-layer model), found by arithmetic from the index.
+ *
+ * Layout of `base`: [num_layers][2 (K, V)][num_blocks][Hkv][block_size][D];
+ * layer l's k_pool is region 2l and its v_pool region 2l+1, each a one-layer
+ * pool as above.
+ *
+ * kvattn_layered_cache_bytes: bytes of that allocation (0 for invalid
+ * arguments or a size that overflows).
+ * kvattn_layer_cache: fills *out with layer `layer`'s one-layer cache (host
+ * arithmetic only, nothing launched; base is a device pointer, 16-byte
+ * aligned).  Errors: INVALID_ARG (null pointer, layer outside
+ * [0, num_layers), num_blocks <= 0, block_size <= 0, misaligned base),
+ * UNSUPPORTED (head_dim, group size).
+ */
+size_t kvattn_layered_cache_bytes(const kvattn_config* cfg, int32_t num_layers, int64_t num_blocks,
+                                  int32_t block_size);
+kvattn_status kvattn_layer_cache(const kvattn_config* cfg, void* base, int32_t num_layers, int64_t num_blocks,
+                                 int32_t block_size, int32_t layer, kvattn_cache* out);
+
+/*
  * Workspace bytes kvattn_decode needs for `batch` sequences of at most
  * max_seq_len tokens with num_splits KV splits (0 = the library's choice for
  * the current device; the same arguments give the same choice).

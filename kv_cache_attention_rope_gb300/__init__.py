@@ -39,6 +39,7 @@ EXPORTED = [
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
     "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
     "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
+    "kvattn_layered_cache_bytes", "kvattn_layer_cache",
 ]
 
 
@@ -73,6 +74,8 @@ def _load():
         "kvattn_rope_append": ([cfgp, cachep, p, p, p, p, p, p, i32, i32, i32, p], ctypes.c_int),
         "kvattn_rope_append_strided": ([cfgp, cachep, p, i64, p, i64, p, i64, p, p, p, p, i32, i32, i32, p],
                                        ctypes.c_int),
+        "kvattn_layered_cache_bytes": ([cfgp, i32, i64, i32], sz),
+        "kvattn_layer_cache": ([cfgp, p, i32, i64, i32, i32, cachep], ctypes.c_int),
         "kvattn_decode_workspace_size": ([cfgp, i32, i32, i32], sz),
         "kvattn_decode_num_splits": ([cfgp, i32, i32, i32], i32),
         "kvattn_decode": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p, sz, p], ctypes.c_int),
@@ -174,6 +177,44 @@ class Cache:
         k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=dtype, device=device)
         v = torch.empty_like(k)
         return cls(k, v)
+
+
+class LayeredCache:
+    """Every layer's K and V pools in one device allocation,
+    [num_layers, 2, num_blocks, Hkv, block_size, D]: one block id (one block
+    table, one allocator) names the same block in all 2 * num_layers regions.
+    layer(l) is that layer's Cache, placed by kvattn_layer_cache."""
+
+    def __init__(self, cfg: Config, pool):
+        if pool.dim() != 6 or pool.shape[1] != 2:
+            raise ValueError("pool must be [num_layers, 2, num_blocks, Hkv, block_size, D]")
+        L, _, nb, hkv, bs, d = pool.shape
+        if (hkv, d) != (cfg.num_kv_heads, cfg.head_dim):
+            raise ValueError("pool heads / head_dim do not match the config")
+        _dev(pool, "pool")
+        need = int(lib.kvattn_layered_cache_bytes(ctypes.byref(cfg), L, nb, bs))
+        if need != pool.numel() * pool.element_size():
+            raise ValueError(f"pool holds {pool.numel() * pool.element_size()} bytes, the layout needs {need}")
+        self.cfg, self.pool = cfg, pool
+        self.num_layers, self.num_blocks, self.block_size = int(L), int(nb), int(bs)
+
+    @classmethod
+    def empty(cls, cfg: Config, num_layers: int, num_blocks: int, block_size: int, dtype, device="cuda"):
+        torch = _torch()
+        pool = torch.empty((num_layers, 2, num_blocks, cfg.num_kv_heads, block_size, cfg.head_dim),
+                           dtype=dtype, device=device)
+        return cls(cfg, pool)
+
+    def layer(self, l: int) -> "Cache":
+        desc = CacheDesc()
+        check(lib.kvattn_layer_cache(ctypes.byref(self.cfg), ctypes.c_void_p(self.pool.data_ptr()),
+                                     self.num_layers, self.num_blocks, self.block_size, int(l),
+                                     ctypes.byref(desc)), "kvattn_layer_cache")
+        c = Cache(self.pool[l, 0], self.pool[l, 1])
+        if (c.desc.k_pool, c.desc.v_pool) != (desc.k_pool, desc.v_pool):
+            raise RuntimeError("kvattn_layer_cache placed the layer away from the pool's [l, 0] / [l, 1] slices")
+        c.desc = desc
+        return c
 
 
 def _rows(t, name: str, heads: int, head_dim: int, dtype=None):

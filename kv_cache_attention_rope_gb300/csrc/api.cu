@@ -224,6 +224,44 @@ kvattn_status kvattn_rope_append_strided(const kvattn_config* cfg, const kvattn_
     return launch_rope_append(a, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// bytes of one layer's K (or V) region, 0 if invalid or too large
+int64_t layer_region_bytes(const kvattn_config* cfg, int32_t num_layers, int64_t num_blocks, int32_t block_size)
+{
+    if (!config_ok(cfg) || num_layers <= 0 || num_blocks <= 0 || block_size <= 0) return 0;
+    const int64_t e = cfg->dtype == KVATTN_BF16 ? 2 : 4;
+    const int64_t per_block = (int64_t)cfg->num_kv_heads * block_size * cfg->head_dim * e;
+    if (per_block <= 0 || num_blocks > INT64_MAX / 4 / per_block / (2 * (int64_t)num_layers)) return 0;
+    return num_blocks * per_block;
+}
+
+}  // namespace
+
+size_t kvattn_layered_cache_bytes(const kvattn_config* cfg, int32_t num_layers, int64_t num_blocks,
+                                  int32_t block_size)
+{
+    const int64_t region = layer_region_bytes(cfg, num_layers, num_blocks, block_size);
+    return region ? (size_t)(region * 2 * num_layers) : 0;
+}
+
+kvattn_status kvattn_layer_cache(const kvattn_config* cfg, void* base, int32_t num_layers, int64_t num_blocks,
+                                 int32_t block_size, int32_t layer, kvattn_cache* out)
+{
+    if (!out || !base || layer < 0 || layer >= num_layers) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return KVATTN_ERR_INVALID_ARG;
+    const int64_t region = layer_region_bytes(cfg, num_layers, num_blocks, block_size);
+    if (!region) return KVATTN_ERR_INVALID_ARG;
+    const kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    char* b = static_cast<char*>(base);
+    out->k_pool = b + (2 * (int64_t)layer) * region;
+    out->v_pool = b + (2 * (int64_t)layer + 1) * region;
+    out->num_blocks = num_blocks;
+    out->block_size = block_size;
+    return KVATTN_OK;
+}
+
 int32_t kvattn_decode_num_splits(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len, int32_t num_splits)
 {
     if (!config_ok(cfg) || config_supported(cfg) != KVATTN_OK || batch < 0 || max_seq_len < 0 || num_splits < 0)

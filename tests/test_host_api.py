@@ -130,6 +130,42 @@ def test_split_qkv_views(kv):
         kv.split_qkv(qkv[:, :-d], hq, hkv, d)
 
 
+def test_layered_cache_placement(kv):
+    """One block id names 2 * L regions: layer l's K area is region 2l, its V area 2l + 1."""
+    E = kv.STATUS_CODE
+    cfg = kv.make_config(32, 8, 128, kv.BF16)
+    L, nb, bs = 4, 1000, 16
+    region = nb * 8 * bs * 128 * 2
+    assert kv.lib.kvattn_layered_cache_bytes(ctypes.byref(cfg), L, nb, bs) == 2 * L * region
+    f32 = kv.make_config(12, 12, 64, kv.F32)
+    assert kv.lib.kvattn_layered_cache_bytes(ctypes.byref(f32), 24, 3, 1025) == 2 * 24 * 3 * 12 * 1025 * 64 * 4
+    base = 0x7F0000000000
+    for layer in range(L):
+        out = kv.CacheDesc()
+        assert kv.lib.kvattn_layer_cache(ctypes.byref(cfg), ctypes.c_void_p(base), L, nb, bs, layer,
+                                         ctypes.byref(out)) == E["KVATTN_OK"]
+        assert out.k_pool == base + 2 * layer * region
+        assert out.v_pool == base + (2 * layer + 1) * region
+        assert (out.num_blocks, out.block_size) == (nb, bs)
+
+    def call(layer=0, b=base, n=nb, L_=L, c=cfg, out=True):
+        o = kv.CacheDesc()
+        return kv.lib.kvattn_layer_cache(ctypes.byref(c), ctypes.c_void_p(b), L_, n, bs, layer,
+                                         ctypes.byref(o) if out else None)
+
+    assert call(layer=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(layer=L) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(b=base + 8) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(b=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(n=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(L_=0) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(out=False) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(c=kv.make_config(32, 8, 96, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]
+    # sizes past int64 are refused, not wrapped
+    assert kv.lib.kvattn_layered_cache_bytes(ctypes.byref(cfg), 1 << 20, 1 << 40, bs) == 0
+    assert call(n=1 << 40, L_=1 << 20) == E["KVATTN_ERR_INVALID_ARG"]
+
+
 def _decode(kv, cfg, cache, B=2, maxlen=64, splits=0, ws=None, ws_bytes=0, out=FAKE, maxb=4):
     return kv.lib.kvattn_decode(ctypes.byref(cfg), ctypes.byref(cache), FAKE, FAKE, maxb, FAKE, B, maxlen,
                                 splits, out, ws, ws_bytes, None)
