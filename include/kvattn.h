@@ -181,6 +181,29 @@ kvattn_status kvattn_layer_cache(const kvattn_config* cfg, void* base, int32_t n
                                  int32_t block_size, int32_t layer, kvattn_cache* out);
 
 /*
+ * kvattn_copy_blocks -- copy-on-write of shared blocks: for i < n, block
+ * dst_ids[i] becomes a bit copy of block src_ids[i], in the K and the V pool
+ * (kvattn_copy_blocks_layered: in every layer's K and V area of a
+ * multi-layer cache, one launch).
+ *
+ * [Nano-vLLM], section 05: blocks carry reference counts so that sequences
+ * with a common prefix share them.  A sequence about to append into a
+ * partially filled block that another sequence also references first gets
+ * its own copy (kvattn_table_prepare_append names the pair), then appends.
+ *
+ *   src_ids, dst_ids  device, [n] int32 block ids
+ * dst ids must be distinct and none of them a src id of the same call.
+ * Errors: INVALID_ARG (null pointer with n > 0, n < 0, bad cache),
+ * UNSUPPORTED, CUDA; device: BAD_INDEX (an id outside the pool: that pair is
+ * skipped).  n == 0 launches nothing.
+ */
+kvattn_status kvattn_copy_blocks(const kvattn_config* cfg, const kvattn_cache* cache, const int32_t* src_ids,
+                                 const int32_t* dst_ids, int32_t n, void* stream);
+kvattn_status kvattn_copy_blocks_layered(const kvattn_config* cfg, void* base, int32_t num_layers,
+                                         int64_t num_blocks, int32_t block_size, const int32_t* src_ids,
+                                         const int32_t* dst_ids, int32_t n, void* stream);
+
+/*
  * Workspace bytes kvattn_decode needs for `batch` sequences of at most
  * max_seq_len tokens with num_splits KV splits (0 = the library's choice for
  * the current device; the same arguments give the same choice).
@@ -346,6 +369,32 @@ kvattn_status kvattn_table_grow(kvattn_allocator* a, int32_t* table_row, int32_t
 /* Frees the blocks covering a sequence of len tokens and sets those entries to -1. */
 kvattn_status kvattn_table_release(kvattn_allocator* a, int32_t* table_row, int32_t max_blocks,
                                    int32_t block_size, int32_t len);
+
+/*
+ * Prefix sharing ([Nano-vLLM], section 05: reference-counted blocks shared by
+ * sequences with a common prefix).  A new sequence starts as the first len
+ * tokens of another: dst_row receives src_row's ids of the blocks covering
+ * len tokens and each gains one reference.  All or nothing; INVALID_ARG for a
+ * block that is not allocated or a row too narrow.
+ */
+kvattn_status kvattn_table_fork(kvattn_allocator* a, const int32_t* src_row, int32_t* dst_row,
+                                int32_t max_blocks, int32_t block_size, int32_t len);
+
+/*
+ * Before appending positions cur_len .. new_len-1 to a sequence: the blocks
+ * of kvattn_table_grow, and copy on write of the block that position cur_len
+ * falls in when that block is already in the row (cur_len % block_size != 0)
+ * and another sequence also references it (refcount > 1).  Then a fresh
+ * block replaces it in the row, the old block loses one reference, and
+ * *cow_src / *cow_dst name the pair for kvattn_copy_blocks, which must run
+ * before the append; otherwise both are -1.  All or nothing: OUT_OF_BLOCKS
+ * (one failure counted) leaves the row and every count as they were.
+ * INVALID_ARG if new_len < cur_len, the row is too narrow, or the block at
+ * cur_len is not allocated.
+ */
+kvattn_status kvattn_table_prepare_append(kvattn_allocator* a, int32_t* table_row, int32_t max_blocks,
+                                          int32_t block_size, int32_t cur_len, int32_t new_len,
+                                          int32_t* cow_src, int32_t* cow_dst);
 
 #ifdef __cplusplus
 }

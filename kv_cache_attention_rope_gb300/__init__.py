@@ -39,7 +39,8 @@ EXPORTED = [
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
     "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
     "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
-    "kvattn_layered_cache_bytes", "kvattn_layer_cache",
+    "kvattn_layered_cache_bytes", "kvattn_layer_cache", "kvattn_copy_blocks", "kvattn_copy_blocks_layered",
+    "kvattn_table_fork", "kvattn_table_prepare_append",
 ]
 
 
@@ -76,6 +77,11 @@ def _load():
                                        ctypes.c_int),
         "kvattn_layered_cache_bytes": ([cfgp, i32, i64, i32], sz),
         "kvattn_layer_cache": ([cfgp, p, i32, i64, i32, i32, cachep], ctypes.c_int),
+        "kvattn_copy_blocks": ([cfgp, cachep, p, p, i32, p], ctypes.c_int),
+        "kvattn_copy_blocks_layered": ([cfgp, p, i32, i64, i32, p, p, i32, p], ctypes.c_int),
+        "kvattn_table_fork": ([p, p, p, i32, i32, i32], ctypes.c_int),
+        "kvattn_table_prepare_append": ([p, p, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+                                        ctypes.c_int),
         "kvattn_decode_workspace_size": ([cfgp, i32, i32, i32], sz),
         "kvattn_decode_num_splits": ([cfgp, i32, i32, i32], i32),
         "kvattn_decode": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p, sz, p], ctypes.c_int),
@@ -215,6 +221,29 @@ class LayeredCache:
             raise RuntimeError("kvattn_layer_cache placed the layer away from the pool's [l, 0] / [l, 1] slices")
         c.desc = desc
         return c
+
+
+def copy_blocks(cfg: Config, cache, src_ids, dst_ids, stream=None) -> None:
+    """kvattn_copy_blocks (a Cache) or kvattn_copy_blocks_layered (a LayeredCache):
+    block dst_ids[i] := block src_ids[i] in every K and V region.  The ids are
+    int32 device tensors, or sequences that are uploaded first."""
+    torch = _torch()
+    dev = cache.pool.device if isinstance(cache, LayeredCache) else cache.k_pool.device
+    src = src_ids if isinstance(src_ids, torch.Tensor) else torch.tensor(list(src_ids), dtype=torch.int32, device=dev)
+    dst = dst_ids if isinstance(dst_ids, torch.Tensor) else torch.tensor(list(dst_ids), dtype=torch.int32, device=dev)
+    if src.numel() != dst.numel():
+        raise ValueError("src_ids and dst_ids differ in length")
+    n = src.numel()
+    if n == 0:
+        return
+    sp, dp = _dev(src, "src_ids", torch.int32), _dev(dst, "dst_ids", torch.int32)
+    if isinstance(cache, LayeredCache):
+        check(lib.kvattn_copy_blocks_layered(ctypes.byref(cfg), ctypes.c_void_p(cache.pool.data_ptr()),
+                                             cache.num_layers, cache.num_blocks, cache.block_size, sp, dp, n,
+                                             _stream(stream)), "kvattn_copy_blocks_layered")
+    else:
+        check(lib.kvattn_copy_blocks(ctypes.byref(cfg), ctypes.byref(cache.desc), sp, dp, n, _stream(stream)),
+              "kvattn_copy_blocks")
 
 
 def _rows(t, name: str, heads: int, head_dim: int, dtype=None):
@@ -400,6 +429,29 @@ class BlockAllocator:
             raise TypeError("table_row must be a contiguous int32 numpy array")
         check(lib.kvattn_table_grow(self._h, table_row.ctypes.data_as(ctypes.c_void_p), table_row.size,
                                     int(block_size), int(cur_len), int(new_len)), "kvattn_table_grow")
+
+    def fork(self, src_row, dst_row, block_size: int, length: int) -> None:
+        """Prefix sharing: dst_row takes src_row's blocks covering `length` tokens
+        (one more reference each)."""
+        for r in (src_row, dst_row):
+            if r.dtype.name != "int32" or not r.flags.c_contiguous:
+                raise TypeError("table rows must be contiguous int32 numpy arrays")
+        if src_row.size != dst_row.size:
+            raise ValueError("rows of different widths")
+        check(lib.kvattn_table_fork(self._h, src_row.ctypes.data_as(ctypes.c_void_p),
+                                    dst_row.ctypes.data_as(ctypes.c_void_p), dst_row.size, int(block_size),
+                                    int(length)), "kvattn_table_fork")
+
+    def prepare_append(self, table_row, block_size: int, cur_len: int, new_len: int):
+        """Blocks for positions cur_len..new_len-1, with copy on write of a shared
+        partial block.  Returns (src, dst) of the block to copy, or None."""
+        if table_row.dtype.name != "int32" or not table_row.flags.c_contiguous:
+            raise TypeError("table_row must be a contiguous int32 numpy array")
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        check(lib.kvattn_table_prepare_append(self._h, table_row.ctypes.data_as(ctypes.c_void_p), table_row.size,
+                                              int(block_size), int(cur_len), int(new_len), ctypes.byref(src),
+                                              ctypes.byref(dst)), "kvattn_table_prepare_append")
+        return None if src.value < 0 else (src.value, dst.value)
 
     def release(self, table_row, block_size: int, length: int) -> None:
         if table_row.dtype.name != "int32" or not table_row.flags.c_contiguous:

@@ -180,4 +180,58 @@ kvattn_status kvattn_table_release(kvattn_allocator* a, int32_t* table_row, int3
     return KVATTN_OK;
 }
 
+kvattn_status kvattn_table_fork(kvattn_allocator* a, const int32_t* src_row, int32_t* dst_row,
+                                int32_t max_blocks, int32_t block_size, int32_t len)
+{
+    if (!a || !src_row || !dst_row || max_blocks <= 0 || block_size <= 0 || len < 0)
+        return KVATTN_ERR_INVALID_ARG;
+    const int32_t have = blocks_for(len, block_size);
+    if (have > max_blocks) return KVATTN_ERR_INVALID_ARG;
+    kvattn_status s = kvattn_share_blocks(a, src_row, have);
+    if (s != KVATTN_OK) return s;
+    std::copy(src_row, src_row + have, dst_row);
+    return KVATTN_OK;
+}
+
+kvattn_status kvattn_table_prepare_append(kvattn_allocator* a, int32_t* table_row, int32_t max_blocks,
+                                          int32_t block_size, int32_t cur_len, int32_t new_len,
+                                          int32_t* cow_src, int32_t* cow_dst)
+{
+    if (!a || !table_row || !cow_src || !cow_dst || max_blocks <= 0 || block_size <= 0 || cur_len < 0 ||
+        new_len < cur_len)
+        return KVATTN_ERR_INVALID_ARG;
+    const int32_t have = blocks_for(cur_len, block_size), need = blocks_for(new_len, block_size);
+    if (need > max_blocks) return KVATTN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(a->mu);
+    // the partially filled block the first new token lands in, if any
+    const bool partial = new_len > cur_len && cur_len % block_size != 0;
+    int32_t old = -1;
+    if (partial) {
+        old = table_row[have - 1];
+        if (old < 0 || (size_t)old >= a->refs.size() || a->refs[(size_t)old] <= 0) return KVATTN_ERR_INVALID_ARG;
+    }
+    const bool cow = partial && a->refs[(size_t)old] > 1;
+    const size_t want = (size_t)(need - have) + (cow ? 1 : 0);
+    if (want > a->free_ids.size()) {
+        ++a->failures;
+        return KVATTN_ERR_OUT_OF_BLOCKS;
+    }
+    auto take = [&]() {
+        const int32_t id = a->free_ids.back();
+        a->free_ids.pop_back();
+        a->refs[(size_t)id] = 1;
+        return id;
+    };
+    *cow_src = *cow_dst = -1;
+    if (cow) {
+        const int32_t fresh = take();
+        --a->refs[(size_t)old];   // still >= 1: another sequence holds it
+        table_row[have - 1] = fresh;
+        *cow_src = old;
+        *cow_dst = fresh;
+    }
+    for (int32_t b = have; b < need; ++b) table_row[b] = take();
+    return KVATTN_OK;
+}
+
 }  // extern "C"

@@ -262,6 +262,56 @@ kvattn_status kvattn_layer_cache(const kvattn_config* cfg, void* base, int32_t n
     return KVATTN_OK;
 }
 
+namespace {
+
+kvattn_status copy_blocks(const kvattn_config* cfg, char* k_base, char* v_base, int64_t layer_stride,
+                          int32_t layers, int64_t num_blocks, int32_t block_size, const int32_t* src_ids,
+                          const int32_t* dst_ids, int32_t n, void* stream)
+{
+    if (n < 0) return KVATTN_ERR_INVALID_ARG;
+    if (n == 0) return KVATTN_OK;
+    if (!src_ids || !dst_ids) return KVATTN_ERR_INVALID_ARG;
+    CopyArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.k_base = k_base;
+    a.v_base = v_base;
+    a.layer_stride = layer_stride;
+    a.layers = layers;
+    a.block_bytes = (int64_t)cfg->num_kv_heads * block_size * cfg->head_dim * (cfg->dtype == KVATTN_BF16 ? 2 : 4);
+    a.num_blocks = num_blocks;
+    a.src = src_ids;
+    a.dst = dst_ids;
+    a.n = n;
+    a.status = device_status_ptr();
+    if (!a.status) return KVATTN_ERR_CUDA;
+    return launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+kvattn_status kvattn_copy_blocks(const kvattn_config* cfg, const kvattn_cache* cache, const int32_t* src_ids,
+                                 const int32_t* dst_ids, int32_t n, void* stream)
+{
+    if (!config_ok(cfg) || !cache_ok(cache, 1)) return KVATTN_ERR_INVALID_ARG;
+    const kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    return copy_blocks(cfg, static_cast<char*>(cache->k_pool), static_cast<char*>(cache->v_pool), 0, 1,
+                       cache->num_blocks, cache->block_size, src_ids, dst_ids, n, stream);
+}
+
+kvattn_status kvattn_copy_blocks_layered(const kvattn_config* cfg, void* base, int32_t num_layers,
+                                         int64_t num_blocks, int32_t block_size, const int32_t* src_ids,
+                                         const int32_t* dst_ids, int32_t n, void* stream)
+{
+    kvattn_cache first;
+    const kvattn_status st = kvattn_layer_cache(cfg, base, num_layers, num_blocks, block_size, 0, &first);
+    if (st != KVATTN_OK) return st;
+    if (num_blocks > INT32_MAX) return KVATTN_ERR_INVALID_ARG;
+    const int64_t region = static_cast<char*>(first.v_pool) - static_cast<char*>(first.k_pool);
+    return copy_blocks(cfg, static_cast<char*>(first.k_pool), static_cast<char*>(first.v_pool), 2 * region,
+                       num_layers, num_blocks, block_size, src_ids, dst_ids, n, stream);
+}
+
 int32_t kvattn_decode_num_splits(const kvattn_config* cfg, int32_t batch, int32_t max_seq_len, int32_t num_splits)
 {
     if (!config_ok(cfg) || config_supported(cfg) != KVATTN_OK || batch < 0 || max_seq_len < 0 || num_splits < 0)

@@ -50,6 +50,23 @@ struct RopeArgs {
 };
 kvattn_status launch_rope_append(const RopeArgs& a, cudaStream_t s);
 
+// Whole-block copies over every K/V region of a (multi-layer) cache: region
+// r = 2 * layer + (0: K, 1: V) starts at (r odd ? v_base : k_base) +
+// layer * layer_stride.
+struct CopyArgs {
+    char* k_base;
+    char* v_base;
+    int64_t layer_stride;   // bytes; 0 for one layer
+    int64_t block_bytes;    // Hkv * block_size * D * element size (a multiple of 16)
+    int64_t num_blocks;
+    const int32_t* src;
+    const int32_t* dst;
+    int32_t n;
+    int32_t layers;
+    int* status;
+};
+kvattn_status launch_copy_blocks(const CopyArgs& a, cudaStream_t s);
+
 struct DecodeArgs {
     const void* q;
     const void* k_pool;

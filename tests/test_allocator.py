@@ -160,3 +160,71 @@ def test_claim_adopts_an_existing_table():
     assert got == {0, 1, 3, 4, 6, 8, 9}
     a.free([2])
     assert a.alloc(1).tolist() == [2]
+
+
+def test_fork_shares_the_prefix_blocks():
+    a = kv.BlockAllocator(16)
+    BS = 16
+    parent = np.full(4, -1, dtype=np.int32)
+    a.grow(parent, BS, 0, 37)                  # 3 blocks, the last one partial
+    child = np.full(4, -1, dtype=np.int32)
+    a.fork(parent, child, BS, 37)
+    assert list(child[:3]) == list(parent[:3]) and child[3] == -1
+    assert [a.refcount(b) for b in parent[:3]] == [2, 2, 2]
+    assert a.num_free == 13
+    # a fork of a block that is not allocated changes nothing
+    bad = np.array([parent[0], 15, -1, -1], dtype=np.int32)
+    with pytest.raises(kv.KvattnError):
+        a.fork(bad, np.full(4, -1, dtype=np.int32), BS, 20)
+    assert a.refcount(parent[0]) == 2
+    with pytest.raises(kv.KvattnError):
+        a.fork(parent, child, BS, 5 * BS)      # wider than the row
+
+
+def test_prepare_append_copies_a_shared_partial_block_once():
+    a = kv.BlockAllocator(16)
+    BS = 16
+    parent = np.full(4, -1, dtype=np.int32)
+    a.grow(parent, BS, 0, 37)
+    child = np.full(4, -1, dtype=np.int32)
+    a.fork(parent, child, BS, 37)
+    shared_last = int(parent[2])
+    # the child appends at position 37, inside the shared block 2: copy on write
+    cow = a.prepare_append(child, BS, 37, 38)
+    assert cow is not None and cow[0] == shared_last and cow[1] != shared_last
+    assert child[2] == cow[1] and a.refcount(cow[1]) == 1 and a.refcount(shared_last) == 1
+    assert list(child[:2]) == list(parent[:2])  # full blocks stay shared
+    # the parent now holds the old block alone: its append writes in place
+    assert a.prepare_append(parent, BS, 37, 38) is None and parent[2] == shared_last
+    # appends that start a block, or append nothing, never copy
+    assert a.prepare_append(child, BS, 38, 48) is None
+    assert a.prepare_append(child, BS, 48, 50) is None and child[3] >= 0
+    assert a.prepare_append(child, BS, 50, 50) is None
+    # releasing both sequences returns every block
+    a.release(child, BS, 50)
+    a.release(parent, BS, 38)
+    assert a.num_free == 16
+
+
+def test_prepare_append_is_all_or_nothing():
+    a = kv.BlockAllocator(4)
+    BS = 16
+    parent = np.full(4, -1, dtype=np.int32)
+    a.grow(parent, BS, 0, 20)                  # 2 blocks
+    child = np.full(4, -1, dtype=np.int32)
+    a.fork(parent, child, BS, 20)
+    before = child.copy()
+    # copy (1 block) + 2 new blocks > 2 free: nothing changes
+    with pytest.raises(kv.KvattnError) as e:
+        a.prepare_append(child, BS, 20, 60)
+    assert e.value.name == "KVATTN_ERR_OUT_OF_BLOCKS"
+    assert np.array_equal(child, before) and a.num_free == 2 and a.num_failures == 1
+    assert a.refcount(parent[1]) == 2
+    # copy + 1 new block fits
+    assert a.prepare_append(child, BS, 20, 40) is not None and a.num_free == 0
+    # a partial block that is not allocated is an error
+    row = np.array([-1, -1, -1, -1], dtype=np.int32)
+    with pytest.raises(kv.KvattnError):
+        a.prepare_append(row, BS, 5, 6)
+    with pytest.raises(kv.KvattnError):
+        a.prepare_append(child, BS, 40, 39)    # shrinking

@@ -166,6 +166,25 @@ def test_layered_cache_placement(kv):
     assert call(n=1 << 40, L_=1 << 20) == E["KVATTN_ERR_INVALID_ARG"]
 
 
+def test_copy_blocks_validation(kv):
+    E = kv.STATUS_CODE
+    cfg = kv.make_config(8, 2, 128, kv.BF16)
+    c = _cache(kv)
+    cp = kv.lib.kvattn_copy_blocks
+    assert cp(ctypes.byref(cfg), ctypes.byref(c), FAKE, FAKE, 0, None) == E["KVATTN_OK"]      # nothing launched
+    assert cp(ctypes.byref(cfg), ctypes.byref(c), FAKE, FAKE, -1, None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert cp(ctypes.byref(cfg), ctypes.byref(c), None, FAKE, 2, None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert cp(ctypes.byref(cfg), None, FAKE, FAKE, 2, None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert cp(ctypes.byref(kv.make_config(8, 2, 80, kv.BF16)), ctypes.byref(c), FAKE, FAKE, 2, None) == \
+        E["KVATTN_ERR_UNSUPPORTED"]
+    lay = kv.lib.kvattn_copy_blocks_layered
+    assert lay(ctypes.byref(cfg), FAKE, 4, 100, 16, FAKE, FAKE, 0, None) == E["KVATTN_OK"]
+    assert lay(ctypes.byref(cfg), FAKE, 0, 100, 16, FAKE, FAKE, 1, None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert lay(ctypes.byref(cfg), ctypes.c_void_p(0x7F0000001008), 4, 100, 16, FAKE, FAKE, 1, None) == \
+        E["KVATTN_ERR_INVALID_ARG"]
+    assert lay(ctypes.byref(cfg), FAKE, 4, 100, 16, FAKE, None, 1, None) == E["KVATTN_ERR_INVALID_ARG"]
+
+
 def _decode(kv, cfg, cache, B=2, maxlen=64, splits=0, ws=None, ws_bytes=0, out=FAKE, maxb=4):
     return kv.lib.kvattn_decode(ctypes.byref(cfg), ctypes.byref(cache), FAKE, FAKE, maxb, FAKE, B, maxlen,
                                 splits, out, ws, ws_bytes, None)
