@@ -85,6 +85,20 @@ typedef struct {
     int32_t block_size;
 } kvattn_cache;
 
+/*
+ * FP8 KV cache (e4m3 codes, 1 byte per element) with one fp32 scale per
+ * (slot, KV head): the value of element d of head h at slot t is
+ * code[t][h][d] * scale[t][h].  Same block layout as kvattn_cache.
+ */
+typedef struct {
+    void* k_pool;          /* device, [num_blocks][Hkv][block_size][D] e4m3 codes */
+    void* v_pool;          /* device, same shape */
+    float* k_scale;        /* device, [num_blocks][Hkv][block_size] */
+    float* v_scale;        /* device, same shape */
+    int64_t num_blocks;
+    int32_t block_size;    /* a multiple of 16 for decode */
+} kvattn_cache_fp8;
+
 /* Library version (KVATTN_VERSION) and a static string for a status code. */
 int32_t kvattn_version(void);
 const char* kvattn_status_string(kvattn_status s);
@@ -202,6 +216,39 @@ kvattn_status kvattn_copy_blocks(const kvattn_config* cfg, const kvattn_cache* c
 kvattn_status kvattn_copy_blocks_layered(const kvattn_config* cfg, void* base, int32_t num_layers,
                                          int64_t num_blocks, int32_t block_size, const int32_t* src_ids,
                                          const int32_t* dst_ids, int32_t n, void* stream);
+
+/*
+ * FP8 KV cache: kvattn_rope_append into a kvattn_cache_fp8, and kvattn_decode
+ * from it (half the bytes per cached token of bf16, plus 8 bytes of scales
+ * per token and KV head).
+ *
+ * [RoPE page], section 2: besides growing with new tokens and being shared
+ * across requests, the KV cache has to support precision compression
+ * (16-bit values quantised to 8 bits).  The decode step reads every cached
+ * byte, so its time scales with the element size.  e4m3 is taken for the
+ * 8-bit format (the GPU converts it to f16 in one instruction per pair).
+ *
+ * kvattn_rope_append_fp8: as kvattn_rope_append (cfg->dtype must be
+ * KVATTN_BF16: q rotated in place in bf16), but each rotated k head row r
+ * (its bf16 values, correctly rounded) and each v head row is stored as
+ *     amax = max |r|,  scale = amax / 448,  inv = 448 / amax   (fp32, RN;
+ *                                                   both 1 when amax = 0)
+ *     code = e4m3_rne_satfinite(r * inv)             (the product in fp32, RN)
+ * with the scale at k_scale / v_scale [block][h][slot].
+ * kvattn_decode_fp8: as kvattn_decode, with K and V the dequantised values
+ * code * scale; bf16 q and output, head_dim 128, group size 4 or 8,
+ * block_size a multiple of 16 (else UNSUPPORTED / INVALID_ARG).  Workspace:
+ * kvattn_decode_workspace_size with the same arguments.
+ * Scale pointers must be 16-byte aligned.
+ */
+kvattn_status kvattn_rope_append_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, void* q,
+                                     const void* k, const void* v, const int32_t* positions, const int32_t* seq_ids,
+                                     const int32_t* block_table, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                     int32_t num_tokens, void* stream);
+kvattn_status kvattn_decode_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, const void* q,
+                                const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /*
  * Workspace bytes kvattn_decode needs for `batch` sequences of at most

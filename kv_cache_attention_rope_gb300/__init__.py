@@ -40,7 +40,7 @@ EXPORTED = [
     "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
     "kvattn_allocator_refcount", "kvattn_table_grow", "kvattn_table_release",
     "kvattn_layered_cache_bytes", "kvattn_layer_cache", "kvattn_copy_blocks", "kvattn_copy_blocks_layered",
-    "kvattn_table_fork", "kvattn_table_prepare_append",
+    "kvattn_table_fork", "kvattn_table_prepare_append", "kvattn_rope_append_fp8", "kvattn_decode_fp8",
 ]
 
 
@@ -62,6 +62,12 @@ class CacheDesc(ctypes.Structure):
                 ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32)]
 
 
+class CacheFP8Desc(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"kvattn CUDA library not built ({LIB_PATH} missing): run "
@@ -78,6 +84,10 @@ def _load():
         "kvattn_layered_cache_bytes": ([cfgp, i32, i64, i32], sz),
         "kvattn_layer_cache": ([cfgp, p, i32, i64, i32, i32, cachep], ctypes.c_int),
         "kvattn_copy_blocks": ([cfgp, cachep, p, p, i32, p], ctypes.c_int),
+        "kvattn_rope_append_fp8": ([cfgp, ctypes.POINTER(CacheFP8Desc), p, p, p, p, p, p, i32, i32, i32, p],
+                                   ctypes.c_int),
+        "kvattn_decode_fp8": ([cfgp, ctypes.POINTER(CacheFP8Desc), p, p, i32, p, i32, i32, i32, p, p, sz, p],
+                              ctypes.c_int),
         "kvattn_copy_blocks_layered": ([cfgp, p, i32, i64, i32, p, p, i32, p], ctypes.c_int),
         "kvattn_table_fork": ([p, p, p, i32, i32, i32], ctypes.c_int),
         "kvattn_table_prepare_append": ([p, p, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
@@ -183,6 +193,60 @@ class Cache:
         k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=dtype, device=device)
         v = torch.empty_like(k)
         return cls(k, v)
+
+
+class CacheFP8:
+    """One layer's fp8 (e4m3) K and V pools, [num_blocks, Hkv, block_size, D]
+    uint8 codes, with one fp32 scale per (block, head, slot)."""
+
+    def __init__(self, k_pool, v_pool, k_scale, v_scale):
+        torch = _torch()
+        if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.dtype != torch.uint8:
+            raise ValueError("k_pool and v_pool must both be uint8 [num_blocks, Hkv, block_size, D]")
+        if k_scale.shape != k_pool.shape[:3] or v_scale.shape != k_scale.shape:
+            raise ValueError("scales must be float32 [num_blocks, Hkv, block_size]")
+        self.k_pool, self.v_pool, self.k_scale, self.v_scale = k_pool, v_pool, k_scale, v_scale
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k_pool.shape
+        self.desc = CacheFP8Desc(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                                 _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+                                 int(self.num_blocks), int(self.block_size))
+
+    @classmethod
+    def empty(cls, num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int, device="cuda"):
+        torch = _torch()
+        k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=torch.uint8, device=device)
+        ks = torch.empty((num_blocks, num_kv_heads, block_size), dtype=torch.float32, device=device)
+        return cls(k, torch.empty_like(k), ks, torch.empty_like(ks))
+
+
+def rope_append_fp8(cfg: Config, cache: CacheFP8, q, k, v, positions, seq_ids, block_table, stream=None) -> None:
+    """kvattn_rope_append_fp8: rotate bf16 q in place, store rotated k and v as e4m3 rows with scales."""
+    torch = _torch()
+    check(lib.kvattn_rope_append_fp8(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q", torch.bfloat16),
+                                     _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16),
+                                     _dev(positions, "positions", torch.int32), _dev(seq_ids, "seq_ids", torch.int32),
+                                     _dev(block_table, "block_table", torch.int32), block_table.shape[0],
+                                     block_table.shape[1], q.shape[0], _stream(stream)),
+          "kvattn_rope_append_fp8")
+
+
+def decode_fp8(cfg: Config, cache: CacheFP8, q, block_table, seq_lens, max_seq_len: int, out=None,
+               workspace=None, num_splits: int = 0, stream=None):
+    """kvattn_decode_fp8: decode attention over an fp8 cache (bf16 q and output)."""
+    torch = _torch()
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = decode_workspace_size(cfg, B, max_seq_len, num_splits)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    check(lib.kvattn_decode_fp8(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q", torch.bfloat16),
+                                _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+                                _dev(seq_lens, "seq_lens", torch.int32), B, int(max_seq_len), int(num_splits),
+                                _dev(out, "out", torch.bfloat16), _dev(workspace, "workspace"), workspace.numel(),
+                                _stream(stream)),
+          "kvattn_decode_fp8")
+    return out
 
 
 class LayeredCache:

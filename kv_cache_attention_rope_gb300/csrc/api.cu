@@ -347,15 +347,27 @@ size_t kvattn_decode_workspace_size(const kvattn_config* cfg, int32_t batch, int
     return workspace_layout(cfg, batch, slots).bytes;
 }
 
-kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,
-                            const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                            int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
-                            size_t workspace_bytes, void* stream)
+namespace {
+
+kvattn_status decode_any(const kvattn_config* cfg, const kvattn_cache* cache, const float* k_scale,
+                         const float* v_scale, const void* q, const int32_t* block_table, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out,
+                         void* workspace, size_t workspace_bytes, void* stream)
 {
     if (!config_ok(cfg) || batch < 0 || max_seq_len < 0 || num_splits < 0) return KVATTN_ERR_INVALID_ARG;
     kvattn_status st = config_supported(cfg);
     if (st != KVATTN_OK) return st;
     if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
+    const bool fp8 = k_scale != nullptr;
+    if (fp8) {
+        if (!v_scale || (reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 15u)
+            return KVATTN_ERR_INVALID_ARG;
+        if (cache->block_size % 16 != 0) return KVATTN_ERR_INVALID_ARG;
+        const int g = cfg->num_q_heads / cfg->num_kv_heads;
+        if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128 || (g != 4 && g != 8)) return KVATTN_ERR_UNSUPPORTED;
+        if ((int64_t)cache->num_blocks * cfg->num_kv_heads * cache->block_size >= ((int64_t)1 << 31))
+            return KVATTN_ERR_UNSUPPORTED;
+    }
     if (batch == 0) return KVATTN_OK;
     if (batch > 8192) return KVATTN_ERR_UNSUPPORTED;
     if (!q || !block_table || !seq_lens || !out) return KVATTN_ERR_INVALID_ARG;
@@ -392,9 +404,84 @@ kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache,
     a.d = cfg->head_dim;
     a.dtype = cfg->dtype;
     a.scale_log2 = scale_of(cfg) * 1.4426950408889634f;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.status = device_status_ptr();
     if (!a.status) return KVATTN_ERR_CUDA;
     return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,
+                            const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream)
+{
+    return decode_any(cfg, cache, nullptr, nullptr, q, block_table, max_blocks_per_seq, seq_lens, batch,
+                      max_seq_len, num_splits, out, workspace, workspace_bytes, stream);
+}
+
+kvattn_status kvattn_decode_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, const void* q,
+                                const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream)
+{
+    if (!cache || !cache->k_scale) return KVATTN_ERR_INVALID_ARG;
+    const kvattn_cache c{cache->k_pool, cache->v_pool, cache->num_blocks, cache->block_size};
+    return decode_any(cfg, &c, cache->k_scale, cache->v_scale, q, block_table, max_blocks_per_seq, seq_lens, batch,
+                      max_seq_len, num_splits, out, workspace, workspace_bytes, stream);
+}
+
+kvattn_status kvattn_rope_append_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, void* q,
+                                     const void* k, const void* v, const int32_t* positions, const int32_t* seq_ids,
+                                     const int32_t* block_table, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                     int32_t num_tokens, void* stream)
+{
+    if (!config_ok(cfg) || num_tokens < 0 || num_seqs <= 0 || !cache) return KVATTN_ERR_INVALID_ARG;
+    kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    if (cfg->dtype != KVATTN_BF16) return KVATTN_ERR_UNSUPPORTED;
+    const kvattn_cache c{cache->k_pool, cache->v_pool, cache->num_blocks, cache->block_size};
+    if (!cache_ok(&c, max_blocks_per_seq) || !cache->k_scale || !cache->v_scale) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cache->k_scale) | reinterpret_cast<uintptr_t>(cache->v_scale)) & 15u)
+        return KVATTN_ERR_INVALID_ARG;
+    if (num_tokens == 0) return KVATTN_OK;
+    if (!q || !k || !v || !positions || !seq_ids || !block_table) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+        return KVATTN_ERR_INVALID_ARG;
+    RopeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const int64_t qrow = (int64_t)cfg->num_q_heads * cfg->head_dim * 2;
+    const int64_t kvrow = (int64_t)cfg->num_kv_heads * cfg->head_dim * 2;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.q_stride = qrow;
+    a.k_stride = kvrow;
+    a.v_stride = kvrow;
+    a.q_out = q;
+    a.q_out_stride = qrow;
+    a.k_pool = cache->k_pool;
+    a.v_pool = cache->v_pool;
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
+    a.positions = positions;
+    a.seq_ids = seq_ids;
+    a.block_table = block_table;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = cache->block_size;
+    a.num_seqs = num_seqs;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_tokens = num_tokens;
+    a.hq = cfg->num_q_heads;
+    a.hkv = cfg->num_kv_heads;
+    a.d = cfg->head_dim;
+    a.dtype = cfg->dtype;
+    a.status = device_status_ptr();
+    if (!a.status) return KVATTN_ERR_CUDA;
+    rope_tables((double)cfg->rope_base, cfg->head_dim, a);
+    return launch_rope_append_fp8(a, static_cast<cudaStream_t>(stream));
 }
 
 kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache* cache, const void* q,

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,6 +30,10 @@ struct RopeArgs {
     int64_t q_stride, k_stride, v_stride;  // bytes from one token's row to the next
     void* q_out;                           // rotated q rows (== q: in place)
     int64_t q_out_stride;                  // bytes
+    // fp8 cache: k_pool / v_pool hold e4m3 codes, these the per-(slot, head)
+    // scales ([num_blocks][Hkv][block_size]); null for a bf16 / fp32 cache
+    float* k_scale;
+    float* v_scale;
     void* k_pool;
     void* v_pool;
     const int32_t* positions;
@@ -49,6 +54,7 @@ struct RopeArgs {
     float4 sector[5];
 };
 kvattn_status launch_rope_append(const RopeArgs& a, cudaStream_t s);
+kvattn_status launch_rope_append_fp8(const RopeArgs& a, cudaStream_t s);  // k_scale / v_scale set
 
 // Whole-block copies over every K/V region of a (multi-layer) cache: region
 // r = 2 * layer + (0: K, 1: V) starts at (r odd ? v_base : k_base) +
@@ -74,6 +80,8 @@ struct DecodeArgs {
     const int32_t* block_table;
     const int32_t* seq_lens;
     void* out;
+    const float* k_scale;  // fp8 cache: per-(slot, head) scales; null otherwise
+    const float* v_scale;
     int32_t* nslots;   // [batch][segments]: pieces each segment was cut into
     float* part_o;     // [batch][hq][splits][d]
     float* part_ml;    // [batch][hq][splits][2] (max in log2 units, sum)

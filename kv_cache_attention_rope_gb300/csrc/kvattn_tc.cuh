@@ -120,6 +120,35 @@ __device__ __forceinline__ void mma_bf16_16816_top(float (&d)[2], uint32_t a0, u
     (void)z3;
 }
 
+// The same with f16 operands (A rows 8..15 zero, C rows 8..15 zero and dropped).
+__device__ __forceinline__ void mma_f16_16816_top(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1)
+{
+    float z2, z3;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %10, %10};"
+        : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    (void)z2;
+    (void)z3;
+}
+
+// two e4m3 codes (low byte = first) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+{
+    uint32_t r;
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(r) : "r"(two));
+    return r;
+}
+
+// f32 pair -> f16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_f16_rn(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // ---- TMA (tensor maps) -----------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* m)
@@ -163,6 +192,10 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int
 // panel][8 rows][128 B]; load a page with tma_load_4d(dst, map, 0, 0, 0,
 // first_row / 8, ...).  False if the driver entry point or the encoding fails.
 bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
+// Host: fp8 pools (one byte per element, 128 per row) as 2-D maps (128 bytes,
+// rows) with a 128 x 16 box, 128-byte swizzle: a 16-row page lands as
+// [row][128 B] with 16-byte chunk c of row r at chunk c ^ (r mod 8).
+bool make_page_maps_fp8(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
 // Host: the same pools as 2-D maps (128 columns, rows) with a 64 x 16 box:
 // two boxes (columns 0 and 64) load 16 rows from any first row into the
 // 128-byte-swizzled layout [64-column panel][16 rows][128 B].

@@ -185,6 +185,36 @@ def test_copy_blocks_validation(kv):
     assert lay(ctypes.byref(cfg), FAKE, 4, 100, 16, FAKE, None, 1, None) == E["KVATTN_ERR_INVALID_ARG"]
 
 
+def test_fp8_cache_validation(kv):
+    E = kv.STATUS_CODE
+    cfg = kv.make_config(32, 8, 128, kv.BF16)
+
+    def c8(bs=16, ks=FAKE, vs=FAKE):
+        return kv.CacheFP8Desc(FAKE, FAKE, ks, vs, 8, bs)
+
+    def dec(c, config=cfg, B=2, out=FAKE):
+        return kv.lib.kvattn_decode_fp8(ctypes.byref(config), ctypes.byref(c) if c is not None else None, FAKE,
+                                        FAKE, 4, FAKE, B, 64, 0, out, FAKE, 1 << 20, None)
+
+    def rope(c, config=cfg, T=1):
+        return kv.lib.kvattn_rope_append_fp8(ctypes.byref(config), ctypes.byref(c) if c is not None else None,
+                                             FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, T, None)
+
+    assert dec(None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert dec(c8(ks=None)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert dec(c8(vs=ctypes.c_void_p(0x7F0000001004))) == E["KVATTN_ERR_INVALID_ARG"]
+    assert dec(c8(bs=24)) == E["KVATTN_ERR_INVALID_ARG"]                      # pages of 16 rows
+    assert dec(c8(), config=kv.make_config(32, 8, 64, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert dec(c8(), config=kv.make_config(16, 8, 128, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]  # group 2
+    assert dec(c8(), config=kv.make_config(32, 8, 128, kv.F32)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert dec(c8(), B=0) == E["KVATTN_OK"]
+    assert dec(c8(), out=None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert rope(None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert rope(c8(ks=None)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert rope(c8(), config=kv.make_config(32, 8, 128, kv.F32)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert rope(c8(), T=0) == E["KVATTN_OK"]
+
+
 def _decode(kv, cfg, cache, B=2, maxlen=64, splits=0, ws=None, ws_bytes=0, out=FAKE, maxb=4):
     return kv.lib.kvattn_decode(ctypes.byref(cfg), ctypes.byref(cache), FAKE, FAKE, maxb, FAKE, B, maxlen,
                                 splits, out, ws, ws_bytes, None)

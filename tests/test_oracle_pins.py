@@ -379,3 +379,76 @@ def test_kv_bytes_closed_form_from_page():
     per_layer = workloads.kv_bytes_read(wl, [gold["tokens"]])
     assert per_layer * gold["layers"] == gold["expect_bytes"] == 2**30
     assert abs(gold["expect_bytes"] / 1e9 - gold["expect_gb_approx"]) < 0.01
+
+
+# --------------------------------------------------------------------------- fp8 (e4m3) cache rows
+
+def test_e4m3_decode_matches_the_format_definition():
+    """Catches a wrong exponent bias, a missing implicit 1, or subnormals
+    decoded as normals: spot codes from the bit layout, and every code against
+    the library's float8_e4m3fn decoding."""
+    from oracle import fp8
+
+    d = fp8.e4m3_decode
+    assert d(0x00) == 0.0 and d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9
+    assert d(0x08) == 2.0 ** -6 and d(0x38) == 1.0 and d(0x39) == 1.125
+    assert d(0x7E) == 448.0 and d(0xFE) == -448.0 and np.isnan(d(0x7F)) and np.isnan(d(0xFF))
+    codes = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    ours = d(codes)
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    ok = ~np.isnan(ours)
+    assert np.array_equal(ours[ok], lib[ok])
+
+
+def test_e4m3_encode_rounding_and_saturation():
+    """Catches round-half-up instead of ties-to-even, truncation, a wrong grid
+    spacing at binade edges, and overflow to NaN instead of saturation."""
+    from oracle import fp8
+
+    e = fp8.e4m3_encode
+    codes = np.arange(256, dtype=np.uint8)
+    vals = fp8.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    # every finite code round-trips (sign of zero included)
+    assert np.array_equal(e(vals[finite]), codes[finite])
+    # ties go to the even mantissa: 1 + 1/16 -> 1.0, 1 + 3/16 -> 1.25, 2^-6 + 2^-10 (subnormal spacing tie) -> 2^-6
+    assert fp8.e4m3_decode(e(1.0625)) == 1.0
+    assert fp8.e4m3_decode(e(1.1875)) == 1.25
+    assert fp8.e4m3_decode(e(2.0 ** -10)) == 0.0 and fp8.e4m3_decode(e(3 * 2.0 ** -10)) == 2 * 2.0 ** -9
+    # just past a tie rounds away from the even neighbour
+    assert fp8.e4m3_decode(e(1.0625 + 2.0 ** -30)) == 1.125
+    # saturation at 448 (no infinities), both signs
+    assert e(500.0) == 0x7E and e(1e30) == 0x7E and e(-1e30) == 0xFE and e(464.0) == 0x7E
+    # against the library's round-to-nearest-even conversion of in-range values
+    g = np.random.default_rng(5)
+    x = np.concatenate([g.standard_normal(20000) * 50, g.standard_normal(20000) * 0.01,
+                        (vals[finite][:-1] + np.diff(vals[finite])[:] / 2)[np.abs(vals[finite][:-1]) < 400]])
+    x = x[np.abs(x) < 448].astype(np.float32).astype(np.float64)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(e(x), lib)
+
+
+def test_fp8_row_quantisation_bounds():
+    """Catches a scale computed from the wrong row, a missing inverse, or codes
+    not saturating: the largest element of a row maps to +-448, and every
+    dequantised value is within half an e4m3 step of the row value."""
+    from oracle import fp8
+
+    g = np.random.default_rng(6)
+    r = torch.from_numpy(g.standard_normal((300, 8, 128)) * np.exp(g.standard_normal((300, 8, 1)))).to(
+        torch.bfloat16).double().numpy()
+    r[0, 0] = 0.0                       # an all-zero row: scale 1, codes 0
+    codes, scale = fp8.quantize_rows(r)
+    assert codes.dtype == np.uint8 and scale.dtype == np.float32 and scale.shape == (300, 8)
+    assert scale[0, 0] == 1.0 and (codes[0, 0] & 0x7F).max() == 0
+    amax = np.abs(r).max(-1)
+    assert np.array_equal(scale[1:], (amax[1:].astype(np.float32) / np.float32(448)))
+    arg = np.abs(r).argmax(-1)
+    top = np.take_along_axis(codes, arg[..., None], -1)[..., 0]
+    assert np.all((top[1:] & 0x7F) == 0x7E)
+    deq = fp8.dequantize_rows(codes, scale)
+    err = np.abs(deq - r)
+    # normal range: half a step is 2^-4 of the magnitude; subnormal: 2^-10 * scale; plus fp32 rounding of r * inv
+    bound = np.maximum(np.abs(r) * 2.0 ** -4, 2.0 ** -10 * scale[..., None].astype(np.float64)) * (1 + 2.0 ** -20)
+    assert np.all(err <= bound + 1e-30)
