@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--layers", type=int, default=1,
                    help="run the step over L layers: one multi-layer cache, each layer's q/k/v taken as views "
                         "of its own fused QKV projection output, rotated q into a dense buffer")
+    p.add_argument("--kv-dtype", choices=["model", "fp8"], default="model",
+                   help="fp8: e4m3 KV cache with a scale per (slot, head) (decode-only workloads)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -173,17 +175,20 @@ class Step:
     """A workload's step on one GPU, inputs resident in HBM."""
 
     def __init__(self, wl: workloads.Workload, device, rows: int = 0, compact_pool: bool = False, chunks: int = -1,
-                 layers: int = 1):
+                 layers: int = 1, kv_fp8: bool = False):
         import torch
 
         import kv_cache_attention_rope_gb300 as kv
 
         self.kv, self.torch, self.wl, self.dev = kv, torch, wl, device
         self.layers = max(1, int(layers))
+        self.fp8 = bool(kv_fp8)
         dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
         self.dt = dt
         H, D, BS = wl.num_kv_heads, wl.head_dim, wl.block_size
         per_block = 2 * BS * H * D * wl.elem_bytes
+        if self.fp8:
+            per_block = 2 * BS * H * (D + 4)   # e4m3 codes + one fp32 scale per (slot, head), K and V
         nb = None
         subset = None
         if rows or chunks >= 0:
@@ -193,6 +198,9 @@ class Step:
                 wl = dataclasses.replace(wl, chunks=nc)
                 self.wl = wl
             subset = list(range(nc)) + list(range(nc, nc + nd))
+        if self.fp8 and (wl.dtype != "bf16" or wl.head_dim != 128 or (wl.chunks and chunks != 0) or self.layers > 1):
+            raise SystemExit("--kv-dtype fp8: bf16 decode-only workloads with head_dim 128, one layer "
+                             "(use --chunks 0 on a mixed workload)")
         if wl.layout == "paged":
             if compact_pool:
                 probe = workloads.make_batch(wl, num_blocks=1 << 30, rows_subset=subset)
@@ -204,7 +212,9 @@ class Step:
         while True:
             batch = workloads.make_batch(wl, num_blocks=nb, rows_subset=subset)
             try:
-                if self.layers == 1:
+                if self.fp8:
+                    self.caches = [kv.CacheFP8.empty(batch.num_blocks, H, BS, device)]
+                elif self.layers == 1:
                     self.caches = [kv.Cache.empty(batch.num_blocks, H, BS, D, dt, device)]
                 else:
                     # one block id names 2 x layers regions of one allocation
@@ -249,7 +259,18 @@ class Step:
         blk = self.table_host[rows, pos // BS].astype(np.int64)
         off = (pos % BS).astype(np.int64)
         step = 1 << 17
-        for c in self.caches:
+        if self.fp8:
+            # every page of a block holding history: finite e4m3 codes of both signs, positive scales
+            used = torch.from_numpy(np.unique(blk)).to(device)
+            pool = self.caches[0].pool
+            for s0 in range(0, len(used), 1 << 14):
+                ids = used[s0:s0 + (1 << 14)]
+                shp = (len(ids),) + tuple(pool.shape[1:3])
+                codes = torch.randint(0, 0x7F, shp + (4096,), generator=gen, device=device, dtype=torch.uint8)
+                sign = torch.randint(0, 2, shp + (4096,), generator=gen, device=device, dtype=torch.uint8)
+                scales = torch.rand(shp + (32,), generator=gen, device=device) * 0.02 + 0.001
+                pool[ids] = torch.cat([codes | (sign << 7), scales.view(torch.uint8)], dim=3)
+        for c in ([] if self.fp8 else self.caches):
             for s in range(0, len(pos), step):
                 b = torch.from_numpy(blk[s:s + step]).to(device)
                 o = torch.from_numpy(off[s:s + step]).to(device)
@@ -314,6 +335,8 @@ class Step:
         E = wl.elem_bytes
         Lr = self.layers
         self.kv_bytes_decode = Lr * workloads.kv_bytes_read(wl, total[nchunk:])
+        if self.fp8:
+            self.kv_bytes_decode = int(np.sum(total[nchunk:])) * 2 * H * (D + 4)
         self.kv_bytes_prefill = Lr * workloads.kv_bytes_read(wl, total[:nchunk])
         self.rope_bytes = Lr * self.n_tok * 2 * (wl.num_q_heads + 2 * H) * D * E
         pre_flops = 0
@@ -345,7 +368,9 @@ class Step:
             e = ev[l] if ev is not None else None
             if e is not None:
                 e[0].record()
-            if self.views:
+            if self.fp8:
+                kv.rope_append_fp8(self.cfg, cache, self.q, self.k, self.v, self.pos, self.sid, self.d_table)
+            elif self.views:
                 q, k, v = self.views[l]
                 kv.rope_append(self.cfg, cache, q, k, v, self.pos, self.sid, self.d_table, q_out=self.q)
             else:
@@ -358,8 +383,8 @@ class Step:
             if e is not None:
                 e[2].record()
             if self.n_dec:
-                kv.decode(self.cfg, cache, self.q_dec, self.d_table_dec, self.lens, self.max_len,
-                          out=self.out_dec, workspace=self.ws)
+                (kv.decode_fp8 if self.fp8 else kv.decode)(self.cfg, cache, self.q_dec, self.d_table_dec, self.lens,
+                                                            self.max_len, out=self.out_dec, workspace=self.ws)
             if e is not None:
                 e[3].record()
         self.alloc_end(ids)
@@ -416,13 +441,15 @@ class Step:
             if i + 1 < steps:
                 self._upload(i + 1)
             cs.wait_event(self.ev_in[b])
-            kv.rope_append(self.cfg, self.cache, d["q"], d["k"], d["v"], d["pos"], d["sid"], d["table"])
+            (kv.rope_append_fp8 if self.fp8 else kv.rope_append)(self.cfg, self.cache, d["q"], d["k"], d["v"],
+                                                                  d["pos"], d["sid"], d["table"])
             if self.nchunk:
                 kv.prefill_chunk(self.cfg, self.cache, d["q_pre"], d["cu"], d["prefix"], d["table_pre"],
                                  self.max_q, out=d["out_pre"])
             if self.n_dec:
-                kv.decode(self.cfg, self.cache, d["q_dec"], d["table_dec"], d["lens"], self.max_len,
-                          out=d["out_dec"], workspace=self.ws)
+                (kv.decode_fp8 if self.fp8 else kv.decode)(self.cfg, self.cache, d["q_dec"], d["table_dec"],
+                                                            d["lens"], self.max_len, out=d["out_dec"],
+                                                            workspace=self.ws)
             self.ev_done[b].record(cs)
             with torch.cuda.stream(xs):
                 xs.wait_event(self.ev_done[b])
@@ -502,7 +529,8 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     wl = workloads.WORKLOADS[args.workload]
-    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool, chunks=args.chunks, layers=args.layers)
+    st = Step(wl, dev, rows=args.rows, compact_pool=args.compact_pool, chunks=args.chunks, layers=args.layers,
+              kv_fp8=args.kv_dtype == "fp8")
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
@@ -570,7 +598,7 @@ def run_ours(args, rank, world):
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": wl.dtype, "data": "synthetic",
+        "dtype": "bf16 q/out, e4m3 KV" if st.fp8 else wl.dtype, "data": "synthetic",
         "config": {"workload": f"{wl.key}: {wl.name}" + (f" (first {args.rows} decode rows)" if args.rows else ""),
                    "decode_seqs": st.n_dec, "prefill_chunks": st.nchunk,
                    "query_tokens": st.n_tok, "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
@@ -580,6 +608,8 @@ def run_ours(args, rank, world):
                    if step_bytes > 2e8 else "L2-resident: KV smaller than L2, not flushed",
                    "parallelism": f"replicas x{world}",
                    "layers": st.layers,
+                   **({"kv_cache": "e4m3 codes + one fp32 scale per (slot, KV head); kv_bytes count both"}
+                      if st.fp8 else {}),
                    **({"qkv_input": "per layer: views of its fused [T, (Hq+2Hkv)D] QKV output; q rotated into "
                                     "a dense buffer; no host upload (e2e measured at layers=1)"}
                       if st.layers > 1 else {})},

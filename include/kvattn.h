@@ -88,15 +88,24 @@ typedef struct {
 /*
  * FP8 KV cache (e4m3 codes, 1 byte per element) with one fp32 scale per
  * (slot, KV head): the value of element d of head h at slot t is
- * code[t][h][d] * scale[t][h].  Same block layout as kvattn_cache.
+ * code[t][h][d] * scale[t][h].  D = 128 only.
+ *
+ * One pool holds K, V and their scales in pages of 16 tokens:
+ *   pool: [num_blocks][Hkv][block_size / 16][4224 bytes]
+ * Page of tokens r = 0..15 (positions 16j + r of the block's group j):
+ *   [0, 2048)     K codes: token r's 16-byte chunk c (dims 16c .. 16c+15)
+ *                 at byte r*128 + 16*(c ^ s(r)),  s(r) = (r & 1) | ((r >> 1) & 6)
+ *   [2048, 4096)  V codes, transposed: dim d of token r at byte 2048 + 16*d + r
+ *   [4096, 4160)  K scales, fp32 [16]
+ *   [4160, 4224)  V scales, fp32 [16]
+ * The decode kernel fetches one page per (16 tokens, KV head) with a single
+ * bulk copy; the chunk rotation and the transposed V make every operand
+ * fragment a conflict-free 32-bit shared-memory load.
  */
 typedef struct {
-    void* k_pool;          /* device, [num_blocks][Hkv][block_size][D] e4m3 codes */
-    void* v_pool;          /* device, same shape */
-    float* k_scale;        /* device, [num_blocks][Hkv][block_size] */
-    float* v_scale;        /* device, same shape */
+    void* pool;            /* device, 16-byte aligned, num_blocks*Hkv*(block_size/16)*4224 bytes */
     int64_t num_blocks;
-    int32_t block_size;    /* a multiple of 16 for decode */
+    int32_t block_size;    /* a multiple of 16 */
 } kvattn_cache_fp8;
 
 /* Library version (KVATTN_VERSION) and a static string for a status code. */
@@ -234,12 +243,11 @@ kvattn_status kvattn_copy_blocks_layered(const kvattn_config* cfg, void* base, i
  *     amax = max |r|,  scale = amax / 448,  inv = 448 / amax   (fp32, RN;
  *                                                   both 1 when amax = 0)
  *     code = e4m3_rne_satfinite(r * inv)             (the product in fp32, RN)
- * with the scale at k_scale / v_scale [block][h][slot].
+ * with its scale, in the page layout of kvattn_cache_fp8 (head_dim 128).
  * kvattn_decode_fp8: as kvattn_decode, with K and V the dequantised values
  * code * scale; bf16 q and output, head_dim 128, group size 4 or 8,
  * block_size a multiple of 16 (else UNSUPPORTED / INVALID_ARG).  Workspace:
  * kvattn_decode_workspace_size with the same arguments.
- * Scale pointers must be 16-byte aligned.
  */
 kvattn_status kvattn_rope_append_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, void* q,
                                      const void* k, const void* v, const int32_t* positions, const int32_t* seq_ids,

@@ -63,9 +63,10 @@ class CacheDesc(ctypes.Structure):
 
 
 class CacheFP8Desc(ctypes.Structure):
-    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
-                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-                ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32)]
+    _fields_ = [("pool", ctypes.c_void_p), ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32)]
+
+
+FP8_PAGE_BYTES = 4224  # one (block, KV head, 16 tokens) page at head_dim 128
 
 
 def _load():
@@ -196,27 +197,28 @@ class Cache:
 
 
 class CacheFP8:
-    """One layer's fp8 (e4m3) K and V pools, [num_blocks, Hkv, block_size, D]
-    uint8 codes, with one fp32 scale per (block, head, slot)."""
+    """One layer's fp8 (e4m3) KV cache: a uint8 pool [num_blocks, Hkv,
+    block_size // 16, 4224] of pages holding 16 tokens' K codes (chunks
+    rotated per row), V codes (transposed) and their per-(slot, head) fp32
+    scales; the byte layout is stated in kvattn.h (kvattn_cache_fp8)."""
 
-    def __init__(self, k_pool, v_pool, k_scale, v_scale):
+    def __init__(self, pool, block_size: int = 16):
         torch = _torch()
-        if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.dtype != torch.uint8:
-            raise ValueError("k_pool and v_pool must both be uint8 [num_blocks, Hkv, block_size, D]")
-        if k_scale.shape != k_pool.shape[:3] or v_scale.shape != k_scale.shape:
-            raise ValueError("scales must be float32 [num_blocks, Hkv, block_size]")
-        self.k_pool, self.v_pool, self.k_scale, self.v_scale = k_pool, v_pool, k_scale, v_scale
-        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k_pool.shape
-        self.desc = CacheFP8Desc(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
-                                 _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
-                                 int(self.num_blocks), int(self.block_size))
+        if pool.dim() != 4 or pool.dtype != torch.uint8 or pool.shape[3] != FP8_PAGE_BYTES:
+            raise ValueError("pool must be uint8 [num_blocks, Hkv, block_size // 16, 4224]")
+        if block_size % 16 or pool.shape[2] != block_size // 16:
+            raise ValueError("block_size must be a multiple of 16 matching the pool's page count")
+        self.pool = pool
+        self.num_blocks, self.num_kv_heads = int(pool.shape[0]), int(pool.shape[1])
+        self.block_size, self.head_dim = int(block_size), 128
+        self.desc = CacheFP8Desc(_dev(pool, "pool"), self.num_blocks, self.block_size)
 
     @classmethod
-    def empty(cls, num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int, device="cuda"):
+    def empty(cls, num_blocks: int, num_kv_heads: int, block_size: int = 16, device="cuda"):
         torch = _torch()
-        k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=torch.uint8, device=device)
-        ks = torch.empty((num_blocks, num_kv_heads, block_size), dtype=torch.float32, device=device)
-        return cls(k, torch.empty_like(k), ks, torch.empty_like(ks))
+        pool = torch.empty((num_blocks, num_kv_heads, block_size // 16, FP8_PAGE_BYTES), dtype=torch.uint8,
+                           device=device)
+        return cls(pool, block_size)
 
 
 def rope_append_fp8(cfg: Config, cache: CacheFP8, q, k, v, positions, seq_ids, block_table, stream=None) -> None:

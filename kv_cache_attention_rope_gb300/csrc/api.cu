@@ -349,8 +349,8 @@ size_t kvattn_decode_workspace_size(const kvattn_config* cfg, int32_t batch, int
 
 namespace {
 
-kvattn_status decode_any(const kvattn_config* cfg, const kvattn_cache* cache, const float* k_scale,
-                         const float* v_scale, const void* q, const int32_t* block_table, int32_t max_blocks_per_seq,
+kvattn_status decode_any(const kvattn_config* cfg, const kvattn_cache* cache, bool fp8,
+                         const void* q, const int32_t* block_table, int32_t max_blocks_per_seq,
                          const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out,
                          void* workspace, size_t workspace_bytes, void* stream)
 {
@@ -358,15 +358,10 @@ kvattn_status decode_any(const kvattn_config* cfg, const kvattn_cache* cache, co
     kvattn_status st = config_supported(cfg);
     if (st != KVATTN_OK) return st;
     if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
-    const bool fp8 = k_scale != nullptr;
     if (fp8) {
-        if (!v_scale || (reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 15u)
-            return KVATTN_ERR_INVALID_ARG;
         if (cache->block_size % 16 != 0) return KVATTN_ERR_INVALID_ARG;
         const int g = cfg->num_q_heads / cfg->num_kv_heads;
         if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128 || (g != 4 && g != 8)) return KVATTN_ERR_UNSUPPORTED;
-        if ((int64_t)cache->num_blocks * cfg->num_kv_heads * cache->block_size >= ((int64_t)1 << 31))
-            return KVATTN_ERR_UNSUPPORTED;
     }
     if (batch == 0) return KVATTN_OK;
     if (batch > 8192) return KVATTN_ERR_UNSUPPORTED;
@@ -404,8 +399,7 @@ kvattn_status decode_any(const kvattn_config* cfg, const kvattn_cache* cache, co
     a.d = cfg->head_dim;
     a.dtype = cfg->dtype;
     a.scale_log2 = scale_of(cfg) * 1.4426950408889634f;
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
+    a.fp8 = fp8 ? 1 : 0;
     a.status = device_status_ptr();
     if (!a.status) return KVATTN_ERR_CUDA;
     return launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -418,8 +412,8 @@ kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache,
                             int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
                             size_t workspace_bytes, void* stream)
 {
-    return decode_any(cfg, cache, nullptr, nullptr, q, block_table, max_blocks_per_seq, seq_lens, batch,
-                      max_seq_len, num_splits, out, workspace, workspace_bytes, stream);
+    return decode_any(cfg, cache, false, q, block_table, max_blocks_per_seq, seq_lens, batch, max_seq_len,
+                      num_splits, out, workspace, workspace_bytes, stream);
 }
 
 kvattn_status kvattn_decode_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, const void* q,
@@ -427,10 +421,10 @@ kvattn_status kvattn_decode_fp8(const kvattn_config* cfg, const kvattn_cache_fp8
                                 int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream)
 {
-    if (!cache || !cache->k_scale) return KVATTN_ERR_INVALID_ARG;
-    const kvattn_cache c{cache->k_pool, cache->v_pool, cache->num_blocks, cache->block_size};
-    return decode_any(cfg, &c, cache->k_scale, cache->v_scale, q, block_table, max_blocks_per_seq, seq_lens, batch,
-                      max_seq_len, num_splits, out, workspace, workspace_bytes, stream);
+    if (!cache) return KVATTN_ERR_INVALID_ARG;
+    const kvattn_cache c{cache->pool, cache->pool, cache->num_blocks, cache->block_size};
+    return decode_any(cfg, &c, true, q, block_table, max_blocks_per_seq, seq_lens, batch, max_seq_len, num_splits,
+                      out, workspace, workspace_bytes, stream);
 }
 
 kvattn_status kvattn_rope_append_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, void* q,
@@ -441,11 +435,9 @@ kvattn_status kvattn_rope_append_fp8(const kvattn_config* cfg, const kvattn_cach
     if (!config_ok(cfg) || num_tokens < 0 || num_seqs <= 0 || !cache) return KVATTN_ERR_INVALID_ARG;
     kvattn_status st = config_supported(cfg);
     if (st != KVATTN_OK) return st;
-    if (cfg->dtype != KVATTN_BF16) return KVATTN_ERR_UNSUPPORTED;
-    const kvattn_cache c{cache->k_pool, cache->v_pool, cache->num_blocks, cache->block_size};
-    if (!cache_ok(&c, max_blocks_per_seq) || !cache->k_scale || !cache->v_scale) return KVATTN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(cache->k_scale) | reinterpret_cast<uintptr_t>(cache->v_scale)) & 15u)
-        return KVATTN_ERR_INVALID_ARG;
+    if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128) return KVATTN_ERR_UNSUPPORTED;
+    const kvattn_cache c{cache->pool, cache->pool, cache->num_blocks, cache->block_size};
+    if (!cache_ok(&c, max_blocks_per_seq) || cache->block_size % 16 != 0) return KVATTN_ERR_INVALID_ARG;
     if (num_tokens == 0) return KVATTN_OK;
     if (!q || !k || !v || !positions || !seq_ids || !block_table) return KVATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
@@ -462,10 +454,9 @@ kvattn_status kvattn_rope_append_fp8(const kvattn_config* cfg, const kvattn_cach
     a.v_stride = kvrow;
     a.q_out = q;
     a.q_out_stride = qrow;
-    a.k_pool = cache->k_pool;
-    a.v_pool = cache->v_pool;
-    a.k_scale = cache->k_scale;
-    a.v_scale = cache->v_scale;
+    a.k_pool = cache->pool;
+    a.v_pool = cache->pool;
+    a.fp8 = 1;
     a.positions = positions;
     a.seq_ids = seq_ids;
     a.block_table = block_table;

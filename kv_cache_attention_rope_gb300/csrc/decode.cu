@@ -132,12 +132,11 @@ struct Traits {
 
 struct SharedLayout {
     int ring_off, merge_off, pbuf_off, prefix_off, bar_off, flag_off, bytes;  // pbuf aliases merge
-    int vscr_off, scale_off;  // fp8 cache: per-warp f16 V page, per-stage K and V scales
 };
 
-// Bytes of one ring stage: K and V pages of a tile (e4m3 codes for an fp8 cache).
+// Bytes of one ring stage: K and V pages of a tile (one fp8 page for an fp8 cache).
 template <bool kBF16, int kD, int kGT, bool kFP8>
-__host__ __device__ constexpr int stage_bytes() { return kFP8 ? 2 * kTile * kD : Traits<kBF16, kD, kGT>::kStageBytes; }
+__host__ __device__ constexpr int stage_bytes() { return kFP8 ? kF8Page : Traits<kBF16, kD, kGT>::kStageBytes; }
 
 template <bool kBF16, int kD, int kGT, bool kFP8 = false>
 __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
@@ -147,13 +146,6 @@ __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
     int off = 0;
     L.ring_off = off;
     off += stages * stage_bytes<kBF16, kD, kGT, kFP8>();
-    L.vscr_off = L.scale_off = 0;
-    if (kFP8) {
-        L.vscr_off = off;                       // 1 KB multiple: the stages are 4 KB
-        off += kConsumerWarps * kTile * kD * 2;
-        L.scale_off = off;
-        off += stages * 2 * kTile * 4;
-    }
     // per consumer warp: its merge slot (kGT x (D + 2) floats, written at the
     // end of a piece) doubles as its probability buffer while tiles stream
     static_assert(T::kTG * T::kV * 8 <= kGT * (kD + 2) * 4, "probability buffer fits the merge slot");
@@ -237,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
     static_assert(!kMma || (kBF16 && kD == 128 && kGT <= 8), "tensor-core path: bf16, D = 128, <= 8 heads");
     static_assert(!kFP8 || (kMma && !kRowBoxes), "fp8 cache: tensor-core path on 16-row pages");
     constexpr int kStageB = stage_bytes<kBF16, kD, kGT, kFP8>();
-    constexpr int kTileB = kStageB / 2;  // K (or V) page of one tile
     extern __shared__ unsigned char smem_raw[];
     // 1 KB alignment: the tensor-core path's stages hold 128-byte-swizzled pages
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -373,13 +364,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
                             const int64_t row = (bj * a.hkv + h) * a.block_size + tok % a.block_size;
                             unsigned char* dst = ring + (size_t)stage * kStageB;
                             if constexpr (kFP8) {
-                                // e4m3 pages (one 128 x 16 box each) and their 16 + 16 scales
-                                float* scl = reinterpret_cast<float*>(smem + SL.scale_off) + stage * 2 * kTile;
-                                mbar_arrive_expect_tx(&full[stage], 2 * kTileB + 2 * kTile * 4);
-                                tma_load_2d(dst, &maps.k, 0, (int)row, &full[stage], policy);
-                                tma_load_2d(dst + kTileB, &maps.v, 0, (int)row, &full[stage], policy);
-                                bulk_load(scl, a.k_scale + row, kTile * 4, &full[stage], policy);
-                                bulk_load(scl + kTile, a.v_scale + row, kTile * 4, &full[stage], policy);
+                                // the fp8 page of these 16 tokens: K, V^T and scales, one copy
+                                const int64_t page = row / kTile;
+                                mbar_arrive_expect_tx(&full[stage], kF8Page);
+                                bulk_load(dst, (const char*)a.k_pool + page * kF8Page, kF8Page, &full[stage], policy);
                             } else if constexpr (kMma) {
                                 // whole 16-row pages (rows past the sequence end are
                                 // masked out of S and zeroed in V by the consumer)
@@ -432,19 +420,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
         const int qh0 = h * G + hsub * kGT;  // first query head of this segment
         float* mw = merge + (size_t)warp * kGT * (kD + 2);
         if constexpr (kFP8) {
-            // ---- fp8 cache on the tensor cores (f16 operands): S = Q K^T with
-            // the dims of each 16-wide k-step permuted so that a lane's four
-            // K values are one 32-bit word of its page row (e4m3 codes, exact
-            // in f16), Q scaled by 2^-4 into f16 range; the K scales multiply
-            // S per token; P is scaled per token by its V scale over a lazy
-            // reference vref, so P V runs on raw V codes, converted to f16 into
-            // this warp's scratch page and read with ldmatrix.trans.
+            // ---- fp8 pages on the tensor cores (f16 operands; e4m3 codes are
+            // exact in f16).  S = Q K^T: MMA 0 takes tokens {4i, 4i+1} and
+            // MMA 1 tokens {4i+2, 4i+3} as its columns, so that lane q4 ends
+            // with the scores of tokens 4q4 .. 4q4+3; the dims of each 16-wide
+            // k-step are permuted so that a lane's four K values are one
+            // 32-bit word.  Q is scaled by 2^-4 into f16 range, the K scales
+            // multiply S per token.  O += P V with the same token order: one
+            // 32-bit word of the transposed V page holds a lane's four tokens
+            // of one dim.  P carries each token's V scale over a lazy
+            // reference vref (rescaled like the running max).
             const int g4 = lane >> 2, q4 = lane & 3;
-            const int mi = lane >> 3, rr = lane & 7;
-            constexpr int gs = 2048, ps = 1024;  // scratch page: [8-row group][64-col panel][8 rows][128 B]
-            unsigned char* vscr = smem + SL.vscr_off + warp * (kTile * kD * 2);
-            const float* sclall = reinterpret_cast<const float*>(smem + SL.scale_off);
-            uint32_t qa[kD / 16][2];  // lane q4 of k-step kk: dims 16kk + 4q4 .. 16kk + 4q4 + 3
+            const int rk0 = (g4 >> 1) * 4 + (g4 & 1), rk1 = rk0 + 2;  // K rows of this lane's columns
+            uint32_t qa[kD / 16][2];  // dims 16kk + 4q4 .. 16kk + 4q4 + 3
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
                 qa[kk][0] = qa[kk][1] = 0u;
@@ -472,56 +460,41 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
                     if (lane == 0) *abort_flag = 1;
                     continue;
                 }
-                const unsigned char* kst = ring + (size_t)stage * kStageB;
-                const unsigned char* vst = kst + kTileB;
-                const float* scl = sclall + stage * 2 * kTile;
+                const unsigned char* pg = ring + (size_t)stage * kStageB;
                 const int tok0 = (pc.t0 + li) * kTile;
                 const int nvalid = min(kTile, pc.len - tok0);
-                // V codes -> f16 scratch page (rows past the sequence end as zeros)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int ci = lane + 32 * j, row = ci >> 3, c16 = ci & 7;
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                    if (row < nvalid) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(vst + row * 128 + ((c16 ^ (row & 7)) << 4));
-                        lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
-                                        e4m3x2_to_f16x2(w.y >> 16));
-                        hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
-                                        e4m3x2_to_f16x2(w.w >> 16));
-                    }
-                    const int cb = 2 * c16;  // f16 chunks cb (dims 16c16..+7) and cb + 1
-                    unsigned char* rowp = vscr + (row >> 3) * gs + (cb >> 3) * ps + (row & 7) * 128;
-                    *reinterpret_cast<uint4*>(rowp + (((cb & 7) ^ (row & 7)) << 4)) = lo;
-                    *reinterpret_cast<uint4*>(rowp + ((((cb + 1) & 7) ^ (row & 7)) << 4)) = hi;
-                }
-                // S: rows g4 (tokens 0-7) and g4 + 8 (tokens 8-15) of the K page
                 float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const int off = ((kk ^ g4) << 4) + 4 * q4;
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kst + g4 * 128 + off);
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kst + (g4 + 8) * 128 + off);
+                    const uint32_t w0 =
+                        *reinterpret_cast<const uint32_t*>(pg + rk0 * 128 + ((kk ^ f8_swz(rk0)) << 4) + 4 * q4);
+                    const uint32_t w1 =
+                        *reinterpret_cast<const uint32_t*>(pg + rk1 * 128 + ((kk ^ f8_swz(rk1)) << 4) + 4 * q4);
                     mma_f16_16816_top(s0, qa[kk][0], qa[kk][1], e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16));
                     mma_f16_16816_top(s1, qa[kk][0], qa[kk][1], e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w1 >> 16));
                 }
-                const int t0 = 2 * q4, t1 = 2 * q4 + 1, t2 = 2 * q4 + 8, t3 = 2 * q4 + 9;
-                float x[4] = {s0[0] * (scl[t0] * sl2), s0[1] * (scl[t1] * sl2), s1[0] * (scl[t2] * sl2),
-                              s1[1] * (scl[t3] * sl2)};
-                float sv[4] = {scl[kTile + t0], scl[kTile + t1], scl[kTile + t2], scl[kTile + t3]};
-                if (t0 >= nvalid) x[0] = -INFINITY, sv[0] = 0.f;
-                if (t1 >= nvalid) x[1] = -INFINITY, sv[1] = 0.f;
-                if (t2 >= nvalid) x[2] = -INFINITY, sv[2] = 0.f;
-                if (t3 >= nvalid) x[3] = -INFINITY, sv[3] = 0.f;
-                __syncwarp();  // scratch written; the stage's pages and scales are no longer read
-                if (lane == 0) mbar_arrive(&empty[stage]);
+                // row g4, tokens 4q4 + {0, 1} (s0) and 4q4 + {2, 3} (s1), in log2 units
+                const float4 ksc = *reinterpret_cast<const float4*>(pg + kF8KsOff + 16 * q4);
+                const float4 vsc4 = *reinterpret_cast<const float4*>(pg + kF8VsOff + 16 * q4);
+                float x[4] = {s0[0] * (ksc.x * sl2), s0[1] * (ksc.y * sl2), s1[0] * (ksc.z * sl2),
+                              s1[1] * (ksc.w * sl2)};
+                float sv[4] = {vsc4.x, vsc4.y, vsc4.z, vsc4.w};
+                uint32_t vmask = 0xffffffffu;  // bytes of this lane's V words that belong to valid tokens
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (4 * q4 + j >= nvalid) {
+                        x[j] = -INFINITY;
+                        sv[j] = 0.f;
+                        vmask &= ~(0xffu << (8 * j));
+                    }
                 float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
                 float vmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
                 vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
                 vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-                // lazy references: the max (rescale when a tile exceeds it by
-                // more than 2^8) and the V scale (when a tile's exceeds it 16x)
+                // lazy references: the max (raised when a tile exceeds it by
+                // more than 2^8) and the V scale (when a tile's is over 16x it)
                 float f = 1.f;
                 if (tmax > m_run + 8.f) {
                     f = m_run == -INFINITY ? 0.f : fast_exp2(m_run - tmax);
@@ -545,16 +518,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma>()) decode_split_ke
                 lrun += (p0 + p1) + (p2 + p3);
                 const uint32_t pa0 = pack_f16_rn(p0 * (sv[0] * vinv), p1 * (sv[1] * vinv));
                 const uint32_t pa2 = pack_f16_rn(p2 * (sv[2] * vinv), p3 * (sv[3] * vinv));
-                const uint32_t vb = smem_addr(vscr);
+                // V^T words: dim 8 nd + g4, tokens 4q4 .. 4q4+3 (stale tokens zeroed: 0 * NaN)
+                const unsigned char* vt = pg + kF8VOff + g4 * 16 + 4 * q4;
 #pragma unroll
-                for (int nd2 = 0; nd2 < kD / 16; ++nd2) {
-                    const int c = 2 * nd2 + (mi >> 1), grp = mi & 1;
-                    uint32_t b[4];
-                    ldmatrix_x4_trans(b, vb + grp * gs + (c >> 3) * ps + rr * 128 + (((c & 7) ^ rr) << 4));
-                    mma_f16_16816_top(o[2 * nd2], pa0, pa2, b[0], b[1]);
-                    mma_f16_16816_top(o[2 * nd2 + 1], pa0, pa2, b[2], b[3]);
+                for (int nd = 0; nd < kD / 8; ++nd) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vt + nd * 128) & vmask;
+                    mma_f16_16816_top(o[nd], pa0, pa2, e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
                 }
-                __syncwarp();  // scratch reads done before the next tile overwrites it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
             }
             pos += ntiles;
             lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
@@ -951,10 +923,7 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
     constexpr int kStageB = stage_bytes<kBF16, kD, kGT, kFP8>();
     PageMaps maps;
     std::memset(&maps, 0, sizeof(maps));
-    if constexpr (kFP8) {
-        if (!make_page_maps_fp8(a.k_pool, a.v_pool, a.num_blocks * a.hkv * a.block_size, &maps.k, &maps.v))
-            return KVATTN_ERR_CUDA;
-    } else if constexpr (kMma) {
+    if constexpr (kMma && !kFP8) {
         const int64_t rows = a.num_blocks * a.hkv * a.block_size;
         if (!(kRowBoxes ? make_row_maps(a.k_pool, a.v_pool, rows, &maps.k, &maps.v)
                         : make_page_maps(a.k_pool, a.v_pool, rows, &maps.k, &maps.v)))
@@ -976,7 +945,7 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
     // mbarrier wait at most one phase away from the phase it names (parity
     // waits cannot tell phase u from phase u - 2).
     const int fixed = shared_layout<kBF16, kD, kGT, kFP8>(0, a.batch).bytes + 1024;  // + base alignment slack
-    const int per_stage = kStageB + (kFP8 ? 2 * kTile * 4 : 0) + 16;  // + scales, + two mbarriers
+    const int per_stage = kStageB + 16;  // + two mbarriers
     const int budget = smem_sm / ctas_per_sm<kMma>() - smem_reserved - fixed;
     int stages = std::min(65536 / kStageB, budget / per_stage);
     stages = std::max(kConsumerWarps, stages / kConsumerWarps * kConsumerWarps);
@@ -1040,7 +1009,7 @@ kvattn_status launch_decode(const DecodeArgs& a, cudaStream_t s)
     const int G = a.hq / a.hkv;
     const bool bf16 = a.dtype == KVATTN_BF16;
     const int gt = G >= 4 ? 4 : G;
-    if (a.k_scale) {  // fp8 cache: the tensor-core path on 16-row pages only
+    if (a.fp8) {  // fp8 pages: the tensor-core path
         if (!(bf16 && a.d == 128 && gt == 4 && a.block_size % 16 == 0)) return KVATTN_ERR_UNSUPPORTED;
         return run<true, 128, 4, true, false, true>(a, s);
     }

@@ -30,10 +30,7 @@ struct RopeArgs {
     int64_t q_stride, k_stride, v_stride;  // bytes from one token's row to the next
     void* q_out;                           // rotated q rows (== q: in place)
     int64_t q_out_stride;                  // bytes
-    // fp8 cache: k_pool / v_pool hold e4m3 codes, these the per-(slot, head)
-    // scales ([num_blocks][Hkv][block_size]); null for a bf16 / fp32 cache
-    float* k_scale;
-    float* v_scale;
+    int32_t fp8;  // k_pool is an fp8 page pool (v_pool unused)
     void* k_pool;
     void* v_pool;
     const int32_t* positions;
@@ -54,7 +51,17 @@ struct RopeArgs {
     float4 sector[5];
 };
 kvattn_status launch_rope_append(const RopeArgs& a, cudaStream_t s);
-kvattn_status launch_rope_append_fp8(const RopeArgs& a, cudaStream_t s);  // k_scale / v_scale set
+kvattn_status launch_rope_append_fp8(const RopeArgs& a, cudaStream_t s);  // a.fp8 set
+
+// fp8 cache page: the 16 tokens of one (block, KV head, 16-token group) at
+// D = 128, laid out for the decode kernel (one bulk copy per page, every
+// fragment load conflict-free):
+//   [0, 2048)     K codes, token r: 16-byte chunk c (dims 16c..16c+15) at
+//                 r * 128 + 16 * (c ^ f8_swz(r))
+//   [2048, 4096)  V codes transposed: dim d, token r at 2048 + 16 * d + r
+//   [4096, 4160)  K scales, fp32 [16];  [4160, 4224) V scales, fp32 [16]
+constexpr int kF8Page = 4224, kF8VOff = 2048, kF8KsOff = 4096, kF8VsOff = 4160;
+__host__ __device__ constexpr int f8_swz(int r) { return (r & 1) | ((r >> 1) & 6); }
 
 // Whole-block copies over every K/V region of a (multi-layer) cache: region
 // r = 2 * layer + (0: K, 1: V) starts at (r odd ? v_base : k_base) +
@@ -80,8 +87,7 @@ struct DecodeArgs {
     const int32_t* block_table;
     const int32_t* seq_lens;
     void* out;
-    const float* k_scale;  // fp8 cache: per-(slot, head) scales; null otherwise
-    const float* v_scale;
+    int32_t fp8;  // k_pool is an fp8 page pool (v_pool unused)
     int32_t* nslots;   // [batch][segments]: pieces each segment was cut into
     float* part_o;     // [batch][hq][splits][d]
     float* part_ml;    // [batch][hq][splits][2] (max in log2 units, sum)

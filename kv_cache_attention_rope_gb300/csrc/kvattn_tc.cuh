@@ -192,10 +192,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int
 // panel][8 rows][128 B]; load a page with tma_load_4d(dst, map, 0, 0, 0,
 // first_row / 8, ...).  False if the driver entry point or the encoding fails.
 bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
-// Host: fp8 pools (one byte per element, 128 per row) as 2-D maps (128 bytes,
-// rows) with a 128 x 16 box, 128-byte swizzle: a 16-row page lands as
-// [row][128 B] with 16-byte chunk c of row r at chunk c ^ (r mod 8).
-bool make_page_maps_fp8(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
 // Host: the same pools as 2-D maps (128 columns, rows) with a 64 x 16 box:
 // two boxes (columns 0 and 64) load 16 rows from any first row into the
 // 128-byte-swizzled layout [64-column panel][16 rows][128 B].

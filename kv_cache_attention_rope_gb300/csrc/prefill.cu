@@ -762,22 +762,6 @@ bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtens
     return true;
 }
 
-bool make_page_maps_fp8(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v)
-{
-    EncodeTiled enc = encoder();
-    if (!enc || rows <= 0 || rows % 16) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kHD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kHD};
-    const cuuint32_t box[2] = {(cuuint32_t)kHD, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    for (int i = 0; i < 2; ++i)
-        if (enc(i ? v : k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(i ? v_pool : k_pool), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return false;
-    return true;
-}
-
 kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
 {
     if (a.d != kHD || a.hq % a.hkv) return KVATTN_ERR_UNSUPPORTED;

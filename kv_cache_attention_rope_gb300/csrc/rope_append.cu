@@ -332,9 +332,10 @@ __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant_
 // for an all-zero row), code = e4m3(r * inv) rounded to nearest even with
 // saturation at +-448.  Dequantised value: code * s.  The lanes sharing one
 // head row (kLanes consecutive lanes, 8 values each) agree on amax with
-// shuffles inside their group.
+// shuffles inside their group.  Returns this lane's 8 codes (first value in
+// the low byte) and the row's scale.
 template <int kLanes>
-__device__ __forceinline__ void store_row_fp8(const uint4& x, unsigned char* dst, float* scale_dst, bool first)
+__device__ __forceinline__ uint2 quant_row_fp8(const uint4& x, float& scale)
 {
     const unsigned lane = threadIdx.x & 31u;
     const unsigned gmask = (kLanes == 32 ? 0xffffffffu : ((1u << kLanes) - 1u) << (lane & ~(unsigned)(kLanes - 1)));
@@ -358,8 +359,26 @@ __device__ __forceinline__ void store_row_fp8(const uint4& x, unsigned char* dst
                                      __NV_SATFINITE, __NV_E4M3);
         w[h] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-    if (first) *scale_dst = sc;
+    scale = sc;
+    return make_uint2(w[0], w[1]);
+}
+
+// This lane's 8 dims (8 * dv ..) of token r's K and V rows into their fp8
+// page (layout: kvattn_internal.cuh, kF8Page); lane dv == 0 writes the scales.
+__device__ __forceinline__ void put_page_fp8(unsigned char* page, int r, int dv, uint2 kc, float ks, uint2 vc,
+                                             float vs)
+{
+    *reinterpret_cast<uint2*>(page + r * 128 + (((dv >> 1) ^ f8_swz(r)) << 4) + (dv & 1) * 8) = kc;
+    unsigned char* vt = page + kF8VOff + (dv * 8) * 16 + r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        vt[(2 * i) * 16] = (unsigned char)((i < 2 ? vc.x : vc.y) >> (16 * (i & 1)));
+        vt[(2 * i + 1) * 16] = (unsigned char)((i < 2 ? vc.x : vc.y) >> (16 * (i & 1) + 8));
+    }
+    if (dv == 0) {
+        reinterpret_cast<float*>(page + kF8KsOff)[r] = ks;
+        reinterpret_cast<float*>(page + kF8VsOff)[r] = vs;
+    }
 }
 
 // ------------------------------------------------------- pipelined variant
@@ -518,18 +537,18 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
             // pool layout [block][kv head][slot][D]: head hg's slot row, this thread's columns
             const unsigned char* ksrc = src + qbytes;
             if constexpr (kFP8) {
-                // e4m3 codes (1 byte per element) and one scale per (slot, head)
-                static_assert(kBF16, "fp8 cache rows are quantised from bf16 inputs");
-                const int64_t srow = ((int64_t)h.blk * a.hkv + hg) * a.block_size + h.off;
-                const int64_t srow_step = (int64_t)kGroups * a.block_size;
-                unsigned char* k8 = (unsigned char*)a.k_pool + srow * kD + dv * kEPV;
-                unsigned char* v8 = (unsigned char*)a.v_pool + srow * kD + dv * kEPV;
+                // e4m3 codes and one scale per (slot, head), in the fp8 page of the token
+                static_assert(kBF16 && kD == 128, "fp8 cache pages hold D = 128 rows quantised from bf16");
+                const int pages = a.block_size / 16;
+                const int64_t page0 = ((int64_t)h.blk * a.hkv + hg) * pages + h.off / 16;
+                unsigned char* pg = (unsigned char*)a.k_pool + page0 * kF8Page;
+                const int64_t step = (int64_t)kGroups * pages * kF8Page;  // kGroups heads further
                 for (int u = 0; u < nk; ++u) {
                     const uint4 x = *reinterpret_cast<const uint4*>(ksrc + u * kHeadStep);
-                    store_row_fp8<kVPH>(rotate16(x), k8 + u * srow_step * kD, a.k_scale + srow + u * srow_step,
-                                        dv == 0);
-                    store_row_fp8<kVPH>(*reinterpret_cast<const uint4*>(ksrc + kbytes + u * kHeadStep),
-                                        v8 + u * srow_step * kD, a.v_scale + srow + u * srow_step, dv == 0);
+                    float ks, vs;
+                    const uint2 kc = quant_row_fp8<kVPH>(rotate16(x), ks);
+                    const uint2 vc = quant_row_fp8<kVPH>(*reinterpret_cast<const uint4*>(ksrc + kbytes + u * kHeadStep), vs);
+                    put_page_fp8(pg + u * step, h.off & 15, dv, kc, ks, vc, vs);
                 }
             } else {
                 const int64_t slot =
@@ -616,7 +635,6 @@ kvattn_status launch_rope_append_fp8(const RopeArgs& a, cudaStream_t s)
     cudaError_t err = cudaSuccess;
     bool launched = false;
     if (a.dtype == KVATTN_BF16 && a.d == 128) launched = launch_pipe<true, 128, true>(a, s, err);
-    else if (a.dtype == KVATTN_BF16 && a.d == 64) launched = launch_pipe<true, 64, true>(a, s, err);
     if (!launched) return KVATTN_ERR_UNSUPPORTED;
     return cuda_status(err);
 }

@@ -28,6 +28,41 @@ def _bf16(a) -> np.ndarray:
     return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
+def _swz(r):
+    return (r & 1) | ((r >> 1) & 6)
+
+
+def pack_pages(ck, sk, cv, sv):
+    """The library's fp8 page layout (kvattn.h, kvattn_cache_fp8) of codes [nb, hkv, BS, 128]
+    and scales [nb, hkv, BS]: [nb, hkv, BS // 16, 4224] bytes."""
+    nb, hkv, bs, D = ck.shape
+    P = bs // 16
+    r = np.arange(16)
+    slot = (r[:, None] * 8 + (np.arange(8)[None, :] ^ _swz(r)[:, None])).reshape(-1)   # (token, chunk) -> slot
+    kpart = np.zeros((nb, hkv, P, 128, 16), np.uint8)
+    kpart[:, :, :, slot, :] = ck.reshape(nb, hkv, P, 128, 16)
+    pages = np.zeros((nb, hkv, P, 4224), np.uint8)
+    pages[..., :2048] = kpart.reshape(nb, hkv, P, 2048)
+    pages[..., 2048:4096] = cv.reshape(nb, hkv, P, 16, D).transpose(0, 1, 2, 4, 3).reshape(nb, hkv, P, 2048)
+    pages[..., 4096:4160] = np.ascontiguousarray(sk.reshape(nb, hkv, P, 16).astype(np.float32)).view(np.uint8)
+    pages[..., 4160:4224] = np.ascontiguousarray(sv.reshape(nb, hkv, P, 16).astype(np.float32)).view(np.uint8)
+    return pages
+
+
+def unpack_rows(pages, blk, off):
+    """Codes [T, hkv, 128] and scales [T, hkv] of K and V at (block, offset) pairs."""
+    T = len(blk)
+    pg = pages[blk, :, off // 16]                       # [T, hkv, 4224]
+    hkv = pg.shape[1]
+    r = off % 16
+    slot = r[:, None] * 8 + (np.arange(8)[None, :] ^ _swz(r)[:, None])
+    ck = np.take_along_axis(pg[..., :2048].reshape(T, hkv, 128, 16), slot[:, None, :, None], axis=2).reshape(T, hkv, 128)
+    cv = np.take_along_axis(pg[..., 2048:4096].reshape(T, hkv, 128, 16), r[:, None, None, None], axis=3)[..., 0]
+    sk = np.ascontiguousarray(pg[..., 4096:4160]).view(np.float32)[np.arange(T), :, r]
+    sv = np.ascontiguousarray(pg[..., 4160:4224]).view(np.float32)[np.arange(T), :, r]
+    return ck, sk, cv, sv
+
+
 def _random_cache(kv, g, nb, hkv, D):
     """Oracle-quantised random rows uploaded as an fp8 cache; dequantised K, V [nb, hkv, BS, D].
     Row magnitudes vary by powers of two (exact in bf16): K over 2^-4 .. 2^2, V over
@@ -38,9 +73,9 @@ def _random_cache(kv, g, nb, hkv, D):
         r = _bf16(g.standard_normal((nb, hkv, BS, D)))
         r *= 2.0 ** g.integers(lo, hi + 1, size=(nb, hkv, BS, 1))
         codes, scale = fp8.quantize_rows(r)
-        parts.append((torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()))
+        parts += [codes, scale]
         deq.append(fp8.dequantize_rows(codes, scale))
-    cache = kv.CacheFP8(parts[0][0], parts[1][0], parts[0][1], parts[1][1])
+    cache = kv.CacheFP8(torch.from_numpy(pack_pages(*parts)).cuda(), BS)
     return cache, deq[0], deq[1]
 
 
@@ -75,7 +110,7 @@ def test_decode_fp8_matches_oracle(kvattn_lib, hq, hkv, splits):
     compare(got[rows], ref, "bf16", f"fp8 decode {hq}/{hkv} splits {splits}")
 
 
-@pytest.mark.parametrize("hq,hkv,D", [(32, 8, 128), (12, 12, 64), (32, 4, 128)])
+@pytest.mark.parametrize("hq,hkv,D", [(32, 8, 128), (12, 12, 128), (32, 4, 128)])
 def test_rope_append_fp8_codes_and_scales_bit_exact(kvattn_lib, hq, hkv, D):
     kv = kvattn_lib
     g = np.random.default_rng(7 + hq + hkv + D)
@@ -98,11 +133,8 @@ def test_rope_append_fp8_codes_and_scales_bit_exact(kvattn_lib, hq, hkv, D):
     v = _bf16(g.standard_normal((T, hkv, D)) * scale_in)
     k[0, 0] = 0.0                                         # an all-zero row: scale 1
     cfg = kv.make_config(hq, hkv, D, kv.BF16)
-    cache = kv.CacheFP8.empty(nb, hkv, BS, D)
-    for p_ in (cache.k_pool, cache.v_pool):
-        p_.fill_(0x7F)
-    for s_ in (cache.k_scale, cache.v_scale):
-        s_.fill_(float("nan"))
+    cache = kv.CacheFP8.empty(nb, hkv, BS)
+    cache.pool.fill_(0x7F)
     bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).cuda()   # noqa: E731
     qd = bf(q)
     kv.rope_append_fp8(cfg, cache, qd, bf(k), bf(v), torch.from_numpy(pos).cuda(), torch.from_numpy(seq).cuda(),
@@ -114,21 +146,23 @@ def test_rope_append_fp8_codes_and_scales_bit_exact(kvattn_lib, hq, hkv, D):
     cv, sv = fp8.quantize_rows(v)
     blk = table[seq, pos // BS].astype(np.int64)
     off = (pos % BS).astype(np.int64)
-    kp, vp = cache.k_pool.cpu().numpy(), cache.v_pool.cpu().numpy()
-    ks, vs = cache.k_scale.cpu().numpy(), cache.v_scale.cpu().numpy()
+    pages = cache.pool.cpu().numpy()
+    gk, gsk, gv, gsv = unpack_rows(pages, blk, off)
     # codes compared with +0 and -0 identified (0x00 / 0x80): the sign of an exact zero
     # from the rotation is not fixed by its definition
     z = lambda c: np.where(c == 0x80, 0, c)   # noqa: E731
-    assert np.array_equal(z(kp[blk, :, off, :]), z(ck))
-    assert np.array_equal(z(vp[blk, :, off, :]), z(cv))
-    assert np.array_equal(ks[blk, :, off].view(np.uint32), sk.view(np.uint32))
-    assert np.array_equal(vs[blk, :, off].view(np.uint32), sv.view(np.uint32))
-    assert ks[blk[0], 0, off[0]] == 1.0
-    # every other slot keeps its sentinel
+    assert np.array_equal(z(gk), z(ck))
+    assert np.array_equal(z(gv), z(cv))
+    assert np.array_equal(gsk.view(np.uint32), sk.view(np.uint32))
+    assert np.array_equal(gsv.view(np.uint32), sv.view(np.uint32))
+    assert gsk[0, 0] == 1.0
+    # every other slot keeps its sentinel bytes
     written = np.zeros((nb, BS), dtype=bool)
     written[blk, off] = True
-    assert np.all(kp.transpose(0, 2, 1, 3)[~written] == 0x7F) and np.all(vp.transpose(0, 2, 1, 3)[~written] == 0x7F)
-    assert np.all(np.isnan(ks.transpose(0, 2, 1)[~written]))
+    ub, uo = np.nonzero(~written)
+    rk, rks, rv, rvs = unpack_rows(pages, ub, uo)
+    assert np.all(rk == 0x7F) and np.all(rv == 0x7F)
+    assert np.all(rks.view(np.uint32) == 0x7F7F7F7F) and np.all(rvs.view(np.uint32) == 0x7F7F7F7F)
 
 
 def test_fp8_history_through_rope_append_then_decode(kvattn_lib):
@@ -147,7 +181,7 @@ def test_fp8_history_through_rope_append_then_decode(kvattn_lib):
     k = _bf16(g.standard_normal((T, hkv, D)))
     v = _bf16(g.standard_normal((T, hkv, D)))
     cfg = kv.make_config(hq, hkv, D, kv.BF16)
-    cache = kv.CacheFP8.empty(nb, hkv, BS, D)
+    cache = kv.CacheFP8.empty(nb, hkv, BS)
     bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).cuda()   # noqa: E731
     qd = bf(q)
     d_table = torch.from_numpy(table).cuda()

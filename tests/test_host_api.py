@@ -189,8 +189,8 @@ def test_fp8_cache_validation(kv):
     E = kv.STATUS_CODE
     cfg = kv.make_config(32, 8, 128, kv.BF16)
 
-    def c8(bs=16, ks=FAKE, vs=FAKE):
-        return kv.CacheFP8Desc(FAKE, FAKE, ks, vs, 8, bs)
+    def c8(bs=16, pool=FAKE):
+        return kv.CacheFP8Desc(pool, 8, bs)
 
     def dec(c, config=cfg, B=2, out=FAKE):
         return kv.lib.kvattn_decode_fp8(ctypes.byref(config), ctypes.byref(c) if c is not None else None, FAKE,
@@ -201,8 +201,8 @@ def test_fp8_cache_validation(kv):
                                              FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, T, None)
 
     assert dec(None) == E["KVATTN_ERR_INVALID_ARG"]
-    assert dec(c8(ks=None)) == E["KVATTN_ERR_INVALID_ARG"]
-    assert dec(c8(vs=ctypes.c_void_p(0x7F0000001004))) == E["KVATTN_ERR_INVALID_ARG"]
+    assert dec(c8(pool=None)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert dec(c8(pool=ctypes.c_void_p(0x7F0000001004))) == E["KVATTN_ERR_INVALID_ARG"]
     assert dec(c8(bs=24)) == E["KVATTN_ERR_INVALID_ARG"]                      # pages of 16 rows
     assert dec(c8(), config=kv.make_config(32, 8, 64, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]
     assert dec(c8(), config=kv.make_config(16, 8, 128, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]  # group 2
@@ -210,7 +210,9 @@ def test_fp8_cache_validation(kv):
     assert dec(c8(), B=0) == E["KVATTN_OK"]
     assert dec(c8(), out=None) == E["KVATTN_ERR_INVALID_ARG"]
     assert rope(None) == E["KVATTN_ERR_INVALID_ARG"]
-    assert rope(c8(ks=None)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert rope(c8(pool=None)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert rope(c8(bs=24)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert rope(c8(), config=kv.make_config(12, 12, 64, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]
     assert rope(c8(), config=kv.make_config(32, 8, 128, kv.F32)) == E["KVATTN_ERR_UNSUPPORTED"]
     assert rope(c8(), T=0) == E["KVATTN_OK"]
 
