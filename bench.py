@@ -592,7 +592,8 @@ def run_ours(args, rank, world):
         by = st.kv_bytes_decode if k == "decode" else st.rope_bytes
         ach = by / parts[k] / 1e9
         return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": measured_traffic(name, wl.key), "peak_source": f"hbm_gbs, {peak_src}"}
+                "traffic": measured_traffic(name, wl.key + ("-fp8" if st.fp8 else "")),
+                "peak_source": f"hbm_gbs, {peak_src}"}
 
     roof = roof_of(dom)
     out = {
