@@ -55,6 +55,9 @@ def parse_args():
                         "of its own fused QKV projection output, rotated q into a dense buffer")
     p.add_argument("--kv-dtype", choices=["model", "fp8"], default="model",
                    help="fp8: e4m3 KV cache with a scale per (slot, head) (decode-only workloads)")
+    p.add_argument("--graph", action="store_true",
+                   help="also time launch-bound small workloads as CUDA-graph replays of 50 steps (L2 warm) "
+                        "and as single steps after an L2 flush")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -523,6 +526,53 @@ def cpu_baseline(wl, target_s: float = 12.0):
             "sample": f"{desc}, {reps} passes in {dt:.1f} s (fp64 C, {cores} threads)"}
 
 
+def graph_timings(st, dev, reps: int = 50, replays: int = 5, flushed_steps: int = 20):
+    """Launch-bound workloads: the step as CUDA-graph replays of `reps` steps
+    (median over `replays`, L2 warm), and single eager steps each after writing
+    a buffer twice the L2 size (median, L2 cold).  The host allocator work of a
+    step is not replayed by the graph (no blocks change hands in these
+    contiguous-cache workloads)."""
+    import torch
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            st.launch()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            st.launch()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(replays):
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    flush = torch.empty(2 * 129 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    cold = []
+    for _ in range(flushed_steps):
+        flush.fill_(1.0)
+        a.record()
+        st.launch()
+        b.record()
+        torch.cuda.synchronize()
+        cold.append(a.elapsed_time(b))
+    status = st.kv.get_device_status()
+    if status:
+        raise RuntimeError(f"device status {st.kv.STATUS.get(status)} in the graph timings")
+    return {"ms_per_step_l2_warm": statistics.median(times), "reps_per_replay": reps, "replays": replays,
+            "ms_per_step_l2_flushed": statistics.median(cold), "flushed_steps": flushed_steps,
+            "launches_per_step": st.launches_per_step}
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -563,6 +613,7 @@ def run_ours(args, rank, world):
     status = st.kv.get_device_status()
     if status:
         raise RuntimeError(f"device status {st.kv.STATUS.get(status)} in the timed region")
+    graph = graph_timings(st, dev) if args.graph else None
     # e2e through host buffers
     e2e = None
     e2e_t = 0.0
@@ -623,6 +674,7 @@ def run_ours(args, rank, world):
         "e2e": e2e,
         "gpu_launches": K * st.launches_per_step,
         "clocks": ck,
+        **({"graph": graph} if graph else {}),
     }
     if st.nchunk:
         out["prefill_tflops"] = st.prefill_flops / t_pre / 1e12
