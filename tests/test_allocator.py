@@ -228,3 +228,74 @@ def test_prepare_append_is_all_or_nothing():
         a.prepare_append(row, BS, 5, 6)
     with pytest.raises(kv.KvattnError):
         a.prepare_append(child, BS, 40, 39)    # shrinking
+
+
+def test_random_sequences_with_forks_against_a_model():
+    """Sequences that grow, fork (shared prefix) and get released, driven
+    through fork / prepare_append / release, checked against a plain model of
+    which block holds which token of which sequence: a token is never written
+    into a block another live sequence still reads, and every count matches."""
+    rng = np.random.default_rng(3)
+    BS, W, n = 16, 12, 160
+    a = kv.BlockAllocator(n)
+    seqs = {}            # id -> (table row, length)
+    next_id = 0
+
+    def refs_model():
+        c = {}
+        for sid, (row, L) in seqs.items():
+            for b in row[: (L + BS - 1) // BS]:
+                c[int(b)] = c.get(int(b), 0) + 1
+        return c
+
+    for _ in range(1500):
+        op = rng.integers(0, 4)
+        if op == 0 or not seqs:                       # new sequence
+            row = np.full(W, -1, dtype=np.int32)
+            L = int(rng.integers(1, 60))
+            try:
+                a.grow(row, BS, 0, L)
+            except kv.KvattnError:
+                continue
+            seqs[next_id] = (row, L)
+            next_id += 1
+        elif op == 1:                                 # fork a prefix of a live sequence
+            sid = int(rng.choice(list(seqs)))
+            row, L = seqs[sid]
+            P = int(rng.integers(1, L + 1))
+            child = np.full(W, -1, dtype=np.int32)
+            a.fork(row, child, BS, P)
+            seqs[next_id] = (child, P)
+            next_id += 1
+        elif op == 2:                                 # append to a sequence
+            sid = int(rng.choice(list(seqs)))
+            row, L = seqs[sid]
+            new = min(W * BS, L + int(rng.integers(1, 40)))
+            if new == L:
+                continue
+            before = row.copy()
+            shared_partial = L % BS != 0 and refs_model().get(int(row[(L - 1) // BS]), 0) > 1
+            try:
+                cow = a.prepare_append(row, BS, L, new)
+            except kv.KvattnError:
+                assert np.array_equal(row, before)    # all or nothing
+                continue
+            assert (cow is not None) == shared_partial
+            if cow is not None:
+                assert cow[0] == before[(L - 1) // BS] and row[(L - 1) // BS] == cow[1]
+            # every block this append writes into is held by this sequence alone
+            seqs[sid] = (row, new)
+            held = refs_model()
+            for blk in row[L // BS: (new + BS - 1) // BS]:
+                assert held[int(blk)] == 1
+        else:                                         # release a sequence
+            sid = int(rng.choice(list(seqs)))
+            row, L = seqs.pop(sid)
+            a.release(row, BS, L)
+        model = refs_model()
+        assert a.num_free == n - len(model)
+        for b, r in model.items():
+            assert a.refcount(b) == r
+    for sid, (row, L) in list(seqs.items()):
+        a.release(row, BS, L)
+    assert a.num_free == n
