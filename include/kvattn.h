@@ -15,7 +15,8 @@
  * Conventions shared by every call
  *   - Pointers documented "device" are CUDA device pointers owned by the
  *     caller; the library never allocates, frees or retains device memory
- *     (the one exception is a 4-byte module-scope device status word).
+ *     (the exceptions are module-scope device variables: a 4-byte status
+ *     word, and the 32 MiB split scratch of kvattn_decode_static_scratch).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  GPU calls are asynchronous on that stream; a returned
  *     KVATTN_OK means the work was validated and launched.
