@@ -110,27 +110,23 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
 // go to scratch registers nothing reads, so they hold no registers across calls.
 __device__ __forceinline__ void mma_bf16_16816_top(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1)
 {
-    float z2, z3;
+    [[maybe_unused]] float z2, z3;
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %10, %10};"
         : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-    (void)z2;
-    (void)z3;
 }
 
 // The same with f16 operands (A rows 8..15 zero, C rows 8..15 zero and dropped).
 __device__ __forceinline__ void mma_f16_16816_top(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1)
 {
-    float z2, z3;
+    [[maybe_unused]] float z2, z3;
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %10, %10};"
         : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-    (void)z2;
-    (void)z3;
 }
 
 // two e4m3 codes (low byte = first) -> f16x2, exact
