@@ -48,3 +48,24 @@ def test_single_process_identity_and_rate():
     assert bench.max_over_ranks([3.0, 4.0]) == [3.0, 4.0]
     # 2 ranks x 10 steps x 1e9 bytes in 4 s -> 5e9 bytes/s
     assert bench.whole_job_rate(1e9, 10, 2, 4.0) == pytest.approx(5e9)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """`bench.py --impl reference` launched as two ranks (the driver's N > 1
+    form): rank 0 alone times the oracle and prints one JSON line; the other
+    rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
