@@ -17,6 +17,9 @@
  *     caller; the library never allocates, frees or retains device memory
  *     (the exceptions are module-scope device variables: a 4-byte status
  *     word, and the 32 MiB split scratch of kvattn_decode_static_scratch).
+ *   - Per-device state (those variables' addresses, kernel attributes,
+ *     tensor maps) is set up on first use with the device current and then
+ *     cached; it is not valid after cudaDeviceReset on that device.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  GPU calls are asynchronous on that stream; a returned
  *     KVATTN_OK means the work was validated and launched.
@@ -314,18 +317,29 @@ kvattn_status kvattn_decode(const kvattn_config* cfg, const kvattn_cache* cache,
  * cudaFree, which would synchronise the device mid-step).  No counterpart on
  * the pages: it is a deployment convenience of this library.
  *
- * Same arguments, results and errors as kvattn_decode, minus the workspace.
- * The partial results live in a fixed 32 MiB array in the library's own
- * device memory (every GPU that loads the library holds it until the process
- * exits); a call whose kvattn_decode_workspace_size(cfg, batch, max_seq_len,
- * num_splits) exceeds 32 MiB returns KVATTN_ERR_WORKSPACE_TOO_SMALL and
- * launches nothing.  The function allocates nothing (no cudaMalloc, cudaFree
- * or allocating library call).  Its first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  All calls on a device
- * share the one array, so calls whose work overlaps on the GPU (different
- * streams, or concurrent host threads) race and must be serialised by the
- * caller.
+ * Same arguments, results and errors as kvattn_decode, minus the workspace
+ * (the checks of kvattn_decode run first, in its order).  The partial results
+ * live in a fixed 32 MiB array in the library's own device memory; a call
+ * whose kvattn_decode_workspace_size(cfg, batch, max_seq_len, num_splits)
+ * exceeds 32 MiB returns KVATTN_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ * The function allocates nothing itself (no cudaMalloc, cudaFree or
+ * allocating library call).
+ *
+ * Placement: the array is placed on a device (32 MiB of its memory, held
+ * until the process exits) by the first call on that device, which also
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current.  Make that first call before sizing your own pools from the free
+ * memory, and before any stream capture: the set-up form
+ *     kvattn_decode_static_scratch(NULL, NULL, NULL, NULL, 0, NULL, 0, 0, 0, NULL, NULL)
+ * (batch 0, cache NULL) does only this and returns KVATTN_OK, or
+ * KVATTN_ERR_CUDA if the device has no room for the array (the runtime error
+ * is cleared).  Later calls reuse the cached address and need no device
+ * memory.  The cached address, like the library's other per-device state,
+ * is not valid after cudaDeviceReset on that device.
+ *
+ * All calls on a device share the one array, so calls whose work overlaps on
+ * the GPU (different streams, or concurrent host threads) race and must be
+ * serialised by the caller.
  */
 kvattn_status kvattn_decode_static_scratch(const kvattn_config* cfg, const kvattn_cache* cache,
                                            const void* q, const int32_t* block_table,

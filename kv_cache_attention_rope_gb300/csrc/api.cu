@@ -56,6 +56,38 @@ int num_sms()
     return g_sms[dev];
 }
 
+bool device_smem(DeviceSmem* out)
+{
+    static DeviceSmem cache[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> g(g_mu);
+    DeviceSmem& c = cache[dev];
+    if (!c.per_sm) {
+        int per_sm = 0, reserved = 0;
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            per_sm <= 0)
+            return false;
+        if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            reserved = 1024;
+        c.reserved = reserved;
+        c.per_sm = per_sm;
+    }
+    *out = c;
+    return true;
+}
+
+cudaError_t SmemLimit::ensure(const void* func, int bytes)
+{
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu_);
+    if (set_[dev] >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) set_[dev] = bytes;
+    return e;
+}
+
 namespace {
 
 bool config_ok(const kvattn_config* c)
@@ -136,6 +168,27 @@ __global__ void selftest_timeout_kernel(int* status, uint64_t limit_ns)
 }
 
 }  // namespace
+
+kvattn_status decode_check(const kvattn_config* cfg, const kvattn_cache* cache, bool fp8, const void* q,
+                           const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t batch, int32_t max_seq_len, int32_t num_splits, const void* out)
+{
+    if (!config_ok(cfg) || batch < 0 || max_seq_len < 0 || num_splits < 0) return KVATTN_ERR_INVALID_ARG;
+    kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
+    if (fp8) {
+        if (cache->block_size % 16 != 0) return KVATTN_ERR_INVALID_ARG;
+        const int g = cfg->num_q_heads / cfg->num_kv_heads;
+        if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128 || (g != 4 && g != 8)) return KVATTN_ERR_UNSUPPORTED;
+    }
+    if (batch == 0) return KVATTN_OK;
+    if (batch > kMaxDecodeBatch) return KVATTN_ERR_UNSUPPORTED;
+    if (!q || !block_table || !seq_lens || !out) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return KVATTN_ERR_INVALID_ARG;
+    return KVATTN_OK;
+}
+
 }  // namespace kvattn
 
 using namespace kvattn;
@@ -354,19 +407,9 @@ kvattn_status decode_any(const kvattn_config* cfg, const kvattn_cache* cache, bo
                          const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t num_splits, void* out,
                          void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (!config_ok(cfg) || batch < 0 || max_seq_len < 0 || num_splits < 0) return KVATTN_ERR_INVALID_ARG;
-    kvattn_status st = config_supported(cfg);
-    if (st != KVATTN_OK) return st;
-    if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
-    if (fp8) {
-        if (cache->block_size % 16 != 0) return KVATTN_ERR_INVALID_ARG;
-        const int g = cfg->num_q_heads / cfg->num_kv_heads;
-        if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128 || (g != 4 && g != 8)) return KVATTN_ERR_UNSUPPORTED;
-    }
-    if (batch == 0) return KVATTN_OK;
-    if (batch > 8192) return KVATTN_ERR_UNSUPPORTED;
-    if (!q || !block_table || !seq_lens || !out) return KVATTN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return KVATTN_ERR_INVALID_ARG;
+    const kvattn_status st = decode_check(cfg, cache, fp8, q, block_table, max_blocks_per_seq, seq_lens, batch,
+                                          max_seq_len, num_splits, out);
+    if (st != KVATTN_OK || batch == 0) return st;
     const DecodePlan p = decode_plan(batch, cfg->num_kv_heads, cfg->num_q_heads / cfg->num_kv_heads, max_seq_len,
                                      num_splits);
     const WorkspaceLayout wl = workspace_layout(cfg, batch, p.slots);

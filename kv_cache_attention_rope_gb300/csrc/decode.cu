@@ -927,21 +927,13 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
     std::memset(&maps, 0, sizeof(maps));
     if constexpr (kMma && !kFP8) {
         const int64_t rows = a.num_blocks * a.hkv * a.block_size;
-        if (!(kRowBoxes ? make_row_maps(a.k_pool, a.v_pool, rows, &maps.k, &maps.v)
-                        : make_page_maps(a.k_pool, a.v_pool, rows, &maps.k, &maps.v)))
-            return KVATTN_ERR_CUDA;
+        if (!pool_maps(a.k_pool, a.v_pool, rows, kRowBoxes, &maps.k, &maps.v)) return KVATTN_ERR_CUDA;
     }
     // Ring depth: as many stages (up to 64 KB of them) as leave room for
     // ctas_per_sm CTAs per SM, counting the per-block reserved shared memory.
-    static int smem_sm = 0, smem_reserved = 0;
-    if (!smem_sm) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
-            return KVATTN_ERR_CUDA;
-        if (cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-            smem_reserved = 1024;
-    }
+    DeviceSmem dsm;
+    if (!device_smem(&dsm)) return KVATTN_ERR_CUDA;
+    const int smem_sm = dsm.per_sm, smem_reserved = dsm.reserved;
     // The depth must be a multiple of the consumer-warp count: then stage s is
     // always consumed by warp s % kConsumerWarps, in order, which keeps every
     // mbarrier wait at most one phase away from the phase it names (parity
@@ -954,16 +946,8 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
     const SharedLayout SL = shared_layout<kBF16, kD, kGT, kFP8>(stages, a.batch);
     const int smem_bytes = SL.bytes + 1024;
     auto kern = decode_split_kernel<kBF16, kD, kGT, kMma, kRowBoxes, kFP8>;
-    static std::mutex mu;
-    static int configured_smem = 0;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        if (smem_bytes > configured_smem) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-            if (e != cudaSuccess) return KVATTN_ERR_CUDA;
-            configured_smem = smem_bytes;
-        }
-    }
+    static SmemLimit limit;
+    if (limit.ensure(reinterpret_cast<const void*>(kern), smem_bytes) != cudaSuccess) return KVATTN_ERR_CUDA;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_bytes) != cudaSuccess)
         return KVATTN_ERR_CUDA;

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "kvattn.h"
 
 namespace kvattn {
@@ -22,6 +24,24 @@ int* device_status_ptr();
 inline kvattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA; }
 
 int num_sms();
+
+// Shared-memory figures of the current device (cached per device).
+struct DeviceSmem {
+    int per_sm;          // cudaDevAttrMaxSharedMemoryPerMultiprocessor
+    int reserved;        // cudaDevAttrReservedSharedMemoryPerBlock
+};
+bool device_smem(DeviceSmem* out);
+
+// A kernel's dynamic shared-memory limit is a per-device attribute: raise it
+// to at least `bytes` on the current device, once per (kernel, device, size).
+class SmemLimit {
+public:
+    cudaError_t ensure(const void* func, int bytes);
+
+private:
+    std::mutex mu_;
+    int set_[64] = {};
+};
 
 struct RopeArgs {
     void* q;
@@ -103,6 +123,15 @@ struct DecodeArgs {
     int* status;
 };
 kvattn_status launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Largest decode batch (the kernels keep a per-sequence prefix sum in shared memory).
+constexpr int32_t kMaxDecodeBatch = 8192;
+
+// Every host-side check of kvattn_decode / kvattn_decode_fp8 that does not
+// involve the workspace, in their order (the same status codes).
+kvattn_status decode_check(const kvattn_config* cfg, const kvattn_cache* cache, bool fp8, const void* q,
+                           const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t batch, int32_t max_seq_len, int32_t num_splits, const void* out);
 
 // Most pieces a (sequence, KV head) segment may be cut into.  splits > 0 is
 // the caller's cap; 0 lets the library choose.  1 = every segment whole.

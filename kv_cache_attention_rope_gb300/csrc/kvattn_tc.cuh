@@ -192,6 +192,9 @@ bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtens
 // two boxes (columns 0 and 64) load 16 rows from any first row into the
 // 128-byte-swizzled layout [64-column panel][16 rows][128 B].
 bool make_row_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtensorMap* k, CUtensorMap* v);
+// Host: make_page_maps (row_boxes false) or make_row_maps (true), with the
+// last few results of the calling thread cached.
+bool pool_maps(const void* k_pool, const void* v_pool, int64_t rows, bool row_boxes, CUtensorMap* k, CUtensorMap* v);
 
 // Warp-level MMA (m16n8k16, bf16 inputs, fp32 accumulate) and its fragment
 // loads from shared memory; layouts as in the PTX ISA description.

@@ -722,7 +722,7 @@ bool make_maps(const PrefillArgs& a, Maps& m)
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
-    return make_page_maps(a.k_pool, a.v_pool, (int64_t)a.num_blocks * a.hkv * a.block_size, &m.k, &m.v);
+    return pool_maps(a.k_pool, a.v_pool, (int64_t)a.num_blocks * a.hkv * a.block_size, false, &m.k, &m.v);
 }
 
 }  // namespace
@@ -762,18 +762,53 @@ bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtens
     return true;
 }
 
+bool pool_maps(const void* k_pool, const void* v_pool, int64_t rows, bool row_boxes, CUtensorMap* k, CUtensorMap* v)
+{
+    // A caller runs the same cache step after step: the last few encodings
+    // of this host thread are kept (a tensor map is a pure function of these
+    // arguments).
+    struct Entry {
+        const void* k_pool;
+        const void* v_pool;
+        int64_t rows;
+        bool row_boxes;
+        CUtensorMap k, v;
+    };
+    constexpr int kEntries = 4;
+    thread_local Entry cache[kEntries];
+    thread_local int filled = 0, next = 0;
+    for (int i = 0; i < filled; ++i) {
+        const Entry& e = cache[i];
+        if (e.k_pool == k_pool && e.v_pool == v_pool && e.rows == rows && e.row_boxes == row_boxes) {
+            *k = e.k;
+            *v = e.v;
+            return true;
+        }
+    }
+    Entry e;
+    if (!(row_boxes ? make_row_maps(k_pool, v_pool, rows, &e.k, &e.v) : make_page_maps(k_pool, v_pool, rows, &e.k, &e.v)))
+        return false;
+    e.k_pool = k_pool;
+    e.v_pool = v_pool;
+    e.rows = rows;
+    e.row_boxes = row_boxes;
+    cache[next] = e;
+    next = (next + 1) % kEntries;
+    filled = filled < kEntries ? filled + 1 : kEntries;
+    *k = e.k;
+    *v = e.v;
+    return true;
+}
+
 kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
 {
     if (a.d != kHD || a.hq % a.hkv) return KVATTN_ERR_UNSUPPORTED;
     if ((int64_t)a.num_blocks * a.hkv * a.block_size >= ((int64_t)1 << 31)) return KVATTN_ERR_UNSUPPORTED;
     Maps maps;
     if (!make_maps(a, maps)) return KVATTN_ERR_CUDA;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return KVATTN_ERR_CUDA;
+    static SmemLimit limit;
+    if (limit.ensure(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes) != cudaSuccess)
+        return KVATTN_ERR_CUDA;
     const int n_qt = (a.max_q_len + 2 * kBM - 1) / (2 * kBM);
     const int64_t items = (int64_t)a.num_chunks * n_qt * a.hq;
     if (items <= 0) return KVATTN_OK;

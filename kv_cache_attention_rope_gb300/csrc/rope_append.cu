@@ -587,16 +587,9 @@ bool launch_pipe(const RopeArgs& a, cudaStream_t s, cudaError_t& err)
     if (stages < 2) return false;
     const int bytes = stages * (int)stage;
     auto kern = rope_append_pipe_kernel<kBF16, kD, kFP8>;
-    static std::mutex mu;
-    static int configured = 0;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        if (bytes > configured) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-            if (err != cudaSuccess) return true;
-            configured = bytes;
-        }
-    }
+    static SmemLimit limit;
+    err = limit.ensure(reinterpret_cast<const void*>(kern), bytes);
+    if (err != cudaSuccess) return true;
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, bytes);
     if (err != cudaSuccess) return true;
