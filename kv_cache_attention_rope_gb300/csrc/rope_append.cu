@@ -35,6 +35,19 @@
 namespace kvattn {
 namespace {
 
+// Register pairs for the packed f32x2 arithmetic of this file, built and split
+// with mov.b64 so that the compiler places the halves without shift/or code.
+__device__ __forceinline__ uint64_t pr(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+    return r;
+}
+__device__ __forceinline__ void pr_halves(uint64_t v, uint32_t& lo, uint32_t& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+
 // ---------------------------------------------------------- float-float
 
 struct ff {
@@ -174,51 +187,71 @@ __device__ __forceinline__ Twiddle2 make_twiddle2(const float4* t)
 {
     const float4 v = *t;
     Twiddle2 w;
-    w.cs = pk(v.x, v.z);
-    w.sc = pk(-v.z, v.x);
+    w.cs = pr(v.x, v.z);
+    w.sc = pr(-v.z, v.x);
     w.ff = t;
     return w;
 }
 
-// Slow path of rotate_bf16_word, kept out of line: it runs for well under one
-// percent of the pairs and would otherwise bloat every inlined copy.
+// Slow path of rotate_bf16_word, kept out of line (it runs for well under one
+// percent of the words and would otherwise bloat every inlined copy), in two
+// levels.
+// First, split twiddles: each component t (cos or sin, |t| <= 1) as
+// t1 + t2 with t1 = t_hi rounded to 16 significant bits and t2 =
+// fl((t_hi - t1) + t_lo), so that |t - t1 - t2| < 2^-39 and a bf16 value (8
+// significant bits) times t1 is exact in fp32.  Then
+//     y0 = fl(fl(x0 c1 - x1 s1) + fl(x0 c2 - fl(x1 s2)))   (y1 alike)
+// has error at most 2^-23 |y| + 5.5 * 2^-39 max(|x0|, |x1|): the roundings of
+// the two partial sums and of y, and the twiddle tail.  A bound relative to
+// |y| decides most of the words that reach this path, by the same test as the
+// fast path with delta = 2^-20 |y| + 2^-36 max|x|.  The rest are rounded from
+// a float-float rotation.
+__device__ __forceinline__ float split_hi16(float hi)
+{
+    return __uint_as_float((__float_as_uint(hi) + 0x80u) & 0xffffff00u);
+}
 __device__ __noinline__ uint32_t rotate_bf16_word_slow(float x0, float x1, float4 ff_cs)
 {
+    const float c1 = split_hi16(ff_cs.x), s1 = split_hi16(ff_cs.z);
+    const float c2 = __fadd_rn(__fsub_rn(ff_cs.x, c1), ff_cs.y), s2 = __fadd_rn(__fsub_rn(ff_cs.z, s1), ff_cs.w);
+    const float y0 = __fadd_rn(__fmaf_rn(-x1, s1, __fmul_rn(x0, c1)), __fmaf_rn(-x1, s2, __fmul_rn(x0, c2)));
+    const float y1 = __fadd_rn(__fmaf_rn(x0, s1, __fmul_rn(x1, c1)), __fmaf_rn(x0, s2, __fmul_rn(x1, c2)));
+    const float d = fmaxf(fmaxf(fabsf(x0), fabsf(x1)) * 0x1p-36f, 0x1p-126f);
+    const float up = 1.0f + 0x1p-20f, dn = 1.0f - 0x1p-20f;
+    const uint32_t hi = pack_bf16_rn(__fmaf_rn(y0, up, copysignf(d, y0)), __fmaf_rn(y1, up, copysignf(d, y1)));
+    const uint32_t lo = pack_bf16_rn(__fmaf_rn(y0, dn, -copysignf(d, y0)), __fmaf_rn(y1, dn, -copysignf(d, y1)));
+    if (hi == lo) return hi;
     ff z0, z1;
     rotate_pair_ff(x0, x1, ff_cs, z0, z1);
     return rne_bf16_ff(z0) | (rne_bf16_ff(z1) << 16);
 }
-
-// Rounding-safety test used below: RNE to bf16 of y is also the RNE of every
-// value within delta of y when the fp32 pattern of y is more than delta away
-// from a bf16 rounding boundary (low 16 bits 0x8000).  Distance in fp32 ulps
-// times |y| over-estimates the distance times 2^23 by at most 2x, hence the
-// conservative test dist * |y| > 2^24 * delta.  Near-zero results fail it and
-// take the slow path.
 
 // Rotates the bf16 pair packed in `w` (low half = even element).
 // Fast path: y = fl(fl(x0 (c, s)) + x1 (-s, c)) with the fp32-rounded
 // twiddle, one packed multiply and one packed fma.  Its error is at most
 // 3 * 2^-24 (|x0| + |x1|): the twiddle's rounding (2^-24 of each term), the
 // product's and the fma's roundings (2^-24 of terms bounded by |x0| + |x1|).
-// With delta = 2^-21 (|x0| + |x1|) a pattern that passes rounding_safe rounds
-// to the correctly rounded rotation.  Otherwise the pair is recomputed in
-// float-float and rounded from there.
+// Rounding test: with delta = 2^-21 (|x0| + |x1|) signed like y, fl(y + delta)
+// and fl(y - delta) must round to the same bf16 value (their own rounding
+// takes at most 2^-24 |y| <= 2^-24 (|x0| + |x1|) off delta, which leaves a
+// margin above the error bound); RNE being monotonic, the exact rotation,
+// within the bound of y, then rounds to that value.  Otherwise (well under
+// one percent of the words, mostly results near zero or near a rounding
+// boundary) the slow path decides.
 __device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const Twiddle2& tw)
 {
     const float x0 = bf16lo(w), x1 = bf16hi(w);
-    const uint64_t y = ffma2(pk(x1, x1), tw.sc, fmul2(pk(x0, x0), tw.cs));
-    const float y0 = pk_lo(y), y1 = pk_hi(y);
-    const float dx = 8.0f * (fabsf(x0) + fabsf(x1));  // 2^24 * 2^-21 * (|x0| + |x1|)
-    // the rounding-safety test for both elements at once: the float with mantissa bits
-    // (low 16 bits of y) | 2^23, minus 2^23 + 2^15, is exactly
-    // (low 16 bits) - 0x8000, so no integer-to-float conversion is needed
-    constexpr float kBias = 8421376.0f;  // 2^23 + 2^15
-    const uint64_t r = fadd2(pk(__uint_as_float((__float_as_uint(y0) & 0xffffu) | 0x4b000000u),
-                                __uint_as_float((__float_as_uint(y1) & 0xffffu) | 0x4b000000u)),
-                             pk(-kBias, -kBias));
-    const uint64_t ry = fmul2(r, y);
-    if (fminf(fabsf(pk_lo(ry)), fabsf(pk_hi(ry))) > dx) return pack_bf16_rn(y0, y1);
+    const uint64_t y = ffma2(pr(x1, x1), tw.sc, fmul2(pr(x0, x0), tw.cs));
+    uint32_t y0, y1;
+    pr_halves(y, y0, y1);
+    const uint32_t dl = __float_as_uint(0x1p-21f * (fabsf(x0) + fabsf(x1)));
+    const uint32_t s0 = y0 & 0x80000000u, s1 = y1 & 0x80000000u;
+    uint32_t a0, a1, b0, b1;
+    pr_halves(fadd2(y, pr(__uint_as_float(dl | s0), __uint_as_float(dl | s1))), a0, a1);
+    pr_halves(fadd2(y, pr(__uint_as_float(dl | (s0 ^ 0x80000000u)), __uint_as_float(dl | (s1 ^ 0x80000000u)))), b0,
+              b1);
+    const uint32_t hi = pack_bf16_rn(__uint_as_float(a0), __uint_as_float(a1));
+    if (hi == pack_bf16_rn(__uint_as_float(b0), __uint_as_float(b1))) return hi;
     return rotate_bf16_word_slow(x0, x1, *tw.ff);
 }
 
