@@ -140,6 +140,12 @@ struct SharedLayout {
 template <bool kBF16, int kD, int kGT, bool kFP8>
 __host__ __device__ constexpr int stage_bytes() { return kFP8 ? kF8Page : Traits<kBF16, kD, kGT>::kStageBytes; }
 
+// Query heads a consumer warp merges per pass (its merge slot's size): a
+// GQA group of 8 on the tensor cores is merged in two passes of 4, which keeps
+// the slot, and with it the ring depth, as for groups of 4.
+template <int kGT>
+__host__ __device__ constexpr int merge_heads() { return kGT < 4 ? kGT : 4; }
+
 template <bool kBF16, int kD, int kGT, bool kFP8 = false>
 __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
 {
@@ -150,9 +156,11 @@ __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
     off += stages * stage_bytes<kBF16, kD, kGT, kFP8>();
     // per consumer warp: its merge slot (kGT x (D + 2) floats, written at the
     // end of a piece) doubles as its probability buffer while tiles stream
-    static_assert(T::kTG * T::kV * 8 <= kGT * (kD + 2) * 4, "probability buffer fits the merge slot");
+    constexpr int kMG = merge_heads<kGT>();
+    static_assert(kMG == kGT || kGT > 4, "only groups above 4 are merged in passes");
+    static_assert(kGT > 4 || T::kTG * T::kV * 8 <= kMG * (kD + 2) * 4, "probability buffer fits the merge slot");
     L.merge_off = off;
-    off += kConsumerWarps * kGT * (kD + 2) * 4;
+    off += kConsumerWarps * kMG * (kD + 2) * 4;
     L.pbuf_off = L.merge_off;
     L.prefix_off = off;
     off += ((batch + 1) * 4 + 15) / 16 * 16;
@@ -411,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
     const int sub = lane % T::kLPG;      // lane inside the group
     const int M = T::mask(sub);          // XOR layout of this lane's partial scores
     const int hm = M / T::kTPG, tm = M % T::kTPG;
-    float2* pbuf = reinterpret_cast<float2*>(merge + (size_t)warp * kGT * (kD + 2)) + grp * T::kV;
+    constexpr int kMG = merge_heads<kGT>();
+    float2* pbuf = reinterpret_cast<float2*>(merge + (size_t)warp * kMG * (kD + 2)) + grp * T::kV;
     const int hq = a.hq;
     uint32_t pos = 0;
     Piece pc;
@@ -420,7 +429,47 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
         const int h = pc.hh / nsub, hsub = pc.hh - h * nsub;
         const int ntiles = pc.t1 - pc.t0;
         const int qh0 = h * G + hsub * kGT;  // first query head of this segment
-        float* mw = merge + (size_t)warp * kGT * (kD + 2);
+        float* mw = merge + (size_t)warp * kMG * (kD + 2);
+        // Merge of the consumer warps' states for query heads h0 .. h0 + kMG - 1
+        // of the segment (each warp has written its state for them into its
+        // slot): the piece's result goes to out, or to its partial slot.
+        auto merge_pass = [&](int h0) {
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            const bool direct = pc.nslots == 1;
+            if (h0 == 0 && tid == 0 && pc.slot == 0 && a.nslots) a.nslots[(int64_t)pc.b * HH + pc.hh] = pc.nslots;
+            for (int e = tid; e < kMG * kD; e += kConsumerWarps * 32) {
+                const int g = e / kD, d = e - g * kD;
+                float Mx = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) Mx = fmaxf(Mx, merge[(w * kMG + g) * (kD + 2) + kD]);
+                float num = 0.f, den = 0.f;
+                if (Mx != -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float* mr = merge + (size_t)(w * kMG + g) * (kD + 2);
+                        const float f = (mr[kD] == -INFINITY) ? 0.f : exp2f(mr[kD] - Mx);
+                        num += f * mr[d];
+                        den += f * mr[kD + 1];
+                    }
+                }
+                const float o = den > 0.f ? num / den : 0.f;
+                const int64_t qrow = (int64_t)pc.b * hq + qh0 + h0 + g;
+                if (direct) {
+                    if constexpr (kBF16)
+                        reinterpret_cast<__nv_bfloat16*>(a.out)[qrow * kD + d] = __float2bfloat16_rn(o);
+                    else
+                        reinterpret_cast<float*>(a.out)[qrow * kD + d] = o;
+                } else {
+                    const int64_t prow = qrow * a.splits + pc.slot;
+                    a.part_o[prow * kD + d] = o;
+                    if (d == 0) {
+                        a.part_ml[prow * 2] = Mx;
+                        a.part_ml[prow * 2 + 1] = den;
+                    }
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        };
         if constexpr (kFP8) {
             // ---- fp8 pages on the tensor cores (f16 operands; e4m3 codes are
             // exact in f16).  S = Q K^T: MMA 0 takes tokens {4i, 4i+1} and
@@ -534,15 +583,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
             lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
             lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
             __syncwarp();
-            if (g4 < kGT) {
 #pragma unroll
-                for (int nd = 0; nd < kD / 8; ++nd)
-                    *reinterpret_cast<float2*>(mw + g4 * (kD + 2) + nd * 8 + 2 * q4) =
-                        make_float2(o[nd][0] * vref, o[nd][1] * vref);
-                if (q4 == 0) {
-                    mw[g4 * (kD + 2) + kD] = m_run;
-                    mw[g4 * (kD + 2) + kD + 1] = lrun;
+            for (int h0 = 0; h0 < kGT; h0 += kMG) {
+                if (g4 >= h0 && g4 < h0 + kMG) {
+                    float* mr = mw + (g4 - h0) * (kD + 2);
+#pragma unroll
+                    for (int nd = 0; nd < kD / 8; ++nd)
+                        *reinterpret_cast<float2*>(mr + nd * 8 + 2 * q4) = make_float2(o[nd][0] * vref, o[nd][1] * vref);
+                    if (q4 == 0) {
+                        mr[kD] = m_run;
+                        mr[kD + 1] = lrun;
+                    }
                 }
+                merge_pass(h0);
             }
         } else if constexpr (kMma) {
             // ---- tensor-core path: S = Q K^T and O += P V as m16n8k16 MMAs
@@ -646,14 +699,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
             lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
             lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
             __syncwarp();
-            if (g4 < kGT) {
 #pragma unroll
-                for (int nd = 0; nd < kD / 8; ++nd)
-                    *reinterpret_cast<float2*>(mw + g4 * (kD + 2) + nd * 8 + 2 * q4) = make_float2(o[nd][0], o[nd][1]);
-                if (q4 == 0) {
-                    mw[g4 * (kD + 2) + kD] = m_run;
-                    mw[g4 * (kD + 2) + kD + 1] = lrun;
+            for (int h0 = 0; h0 < kGT; h0 += kMG) {
+                if (g4 >= h0 && g4 < h0 + kMG) {
+                    float* mr = mw + (g4 - h0) * (kD + 2);
+#pragma unroll
+                    for (int nd = 0; nd < kD / 8; ++nd)
+                        *reinterpret_cast<float2*>(mr + nd * 8 + 2 * q4) = make_float2(o[nd][0], o[nd][1]);
+                    if (q4 == 0) {
+                        mr[kD] = m_run;
+                        mr[kD + 1] = lrun;
+                    }
                 }
+                merge_pass(h0);
             }
         } else {
 
@@ -840,42 +898,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
                 }
             }
         }
+        merge_pass(0);
         }  // CUDA-core path
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        const bool direct = pc.nslots == 1;
-        if (tid == 0 && pc.slot == 0 && a.nslots) a.nslots[(int64_t)pc.b * HH + pc.hh] = pc.nslots;
-        for (int e = tid; e < kGT * kD; e += kConsumerWarps * 32) {
-            const int g = e / kD, d = e - g * kD;
-            float Mx = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) Mx = fmaxf(Mx, merge[(w * kGT + g) * (kD + 2) + kD]);
-            float num = 0.f, den = 0.f;
-            if (Mx != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float* mr = merge + (size_t)(w * kGT + g) * (kD + 2);
-                    const float f = (mr[kD] == -INFINITY) ? 0.f : exp2f(mr[kD] - Mx);
-                    num += f * mr[d];
-                    den += f * mr[kD + 1];
-                }
-            }
-            const float o = den > 0.f ? num / den : 0.f;
-            const int64_t qrow = (int64_t)pc.b * hq + qh0 + g;
-            if (direct) {
-                if constexpr (kBF16)
-                    reinterpret_cast<__nv_bfloat16*>(a.out)[qrow * kD + d] = __float2bfloat16_rn(o);
-                else
-                    reinterpret_cast<float*>(a.out)[qrow * kD + d] = o;
-            } else {
-                const int64_t prow = qrow * a.splits + pc.slot;
-                a.part_o[prow * kD + d] = o;
-                if (d == 0) {
-                    a.part_ml[prow * 2] = Mx;
-                    a.part_ml[prow * 2 + 1] = den;
-                }
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
 }
 
@@ -995,14 +1019,19 @@ kvattn_status launch_decode(const DecodeArgs& a, cudaStream_t s)
     const int G = a.hq / a.hkv;
     const bool bf16 = a.dtype == KVATTN_BF16;
     const int gt = G >= 4 ? 4 : G;
-    if (a.fp8) {  // fp8 pages: the tensor-core path
-        if (!(bf16 && a.d == 128 && gt == 4 && a.block_size % 16 == 0)) return KVATTN_ERR_UNSUPPORTED;
-        return run<true, 128, 4, true, false, true>(a, s);
+    if (a.fp8) {  // fp8 pages: the tensor-core path, every head of the group in one segment
+        if (!(bf16 && a.d == 128 && (G == 4 || G == 8) && a.block_size % 16 == 0)) return KVATTN_ERR_UNSUPPORTED;
+        return G == 8 ? run<true, 128, 8, true, false, true>(a, s) : run<true, 128, 4, true, false, true>(a, s);
     }
-    // bf16, D = 128, groups of 4 query heads per KV head: QK and PV on the
-    // tensor cores (tensor-map row coordinates are 32-bit)
-    if (bf16 && a.d == 128 && gt == 4 && a.num_blocks * a.hkv * a.block_size < ((int64_t)1 << 31))
+    // bf16, D = 128, groups of 4 or 8 query heads per KV head: QK and PV on the
+    // tensor cores with the group's heads as rows 0..G-1 of the MMA fragments,
+    // so every page is read once per KV head (tensor-map row coordinates are
+    // 32-bit)
+    if (bf16 && a.d == 128 && (G == 4 || G == 8) && a.num_blocks * a.hkv * a.block_size < ((int64_t)1 << 31)) {
+        if (G == 8)
+            return a.block_size % 16 == 0 ? run<true, 128, 8, true, false>(a, s) : run<true, 128, 8, true, true>(a, s);
         return a.block_size % 16 == 0 ? run<true, 128, 4, true, false>(a, s) : run<true, 128, 4, true, true>(a, s);
+    }
 #define KVATTN_DECODE_CASE(BF, DD, GG) \
     if (bf16 == BF && a.d == DD && gt == GG) return run<BF, DD, GG, false>(a, s);
     KVATTN_DECODE_CASE(true, 128, 1)

@@ -140,8 +140,10 @@ struct DecodePlan {
 };
 DecodePlan decode_plan(int32_t batch, int32_t hkv, int32_t group, int32_t max_seq_len, int32_t splits);
 
-// Segments per sequence: KV heads, times 2 when a GQA group of 8 is split
-// into two kernels' worth of 4 query heads.
+// Segments per sequence, at most: KV heads, times 2 when a GQA group of 8 is
+// split into two segments of 4 query heads (the CUDA-core path: fp32 caches
+// or D = 64; the tensor-core path keeps a group of 8 in one segment).  Sizes
+// the workspace's piece counts.
 inline int32_t decode_segments(int32_t hq, int32_t hkv)
 {
     const int32_t g = hq / hkv;
