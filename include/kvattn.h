@@ -365,8 +365,9 @@ kvattn_status kvattn_decode_static_scratch(const kvattn_config* cfg, const kvatt
  *   block_table device, [num_chunks][max_blocks_per_seq] int32
  *   max_q_len   host upper bound of cu_q_lens[c+1] - cu_q_lens[c]
  *   out         device, [total_q][Hq][D]
- * Uses the tcgen05 tensor cores; needs block_size % 16 == 0 and
- * head_dim == 128.  Errors: INVALID_ARG, UNSUPPORTED, CUDA; device:
+ * Uses the tcgen05 tensor cores; needs block_size % 16 == 0 (a contiguous
+ * cache then has rows of a multiple of 16 tokens) and head_dim 128 or 64
+ * (the GPT-2 shape).  Errors: INVALID_ARG, UNSUPPORTED, CUDA; device:
  * BAD_INDEX, TIMEOUT.  num_chunks == 0 launches nothing.
  */
 kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache* cache,

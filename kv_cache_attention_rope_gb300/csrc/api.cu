@@ -526,7 +526,7 @@ kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache*
     if (!config_ok(cfg) || num_chunks < 0 || max_q_len < 0 || total_q < 0) return KVATTN_ERR_INVALID_ARG;
     kvattn_status st = config_supported(cfg);
     if (st != KVATTN_OK) return st;
-    if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128) return KVATTN_ERR_UNSUPPORTED;
+    if (cfg->dtype != KVATTN_BF16 || (cfg->head_dim != 128 && cfg->head_dim != 64)) return KVATTN_ERR_UNSUPPORTED;
     if (!cache_ok(cache, max_blocks_per_seq)) return KVATTN_ERR_INVALID_ARG;
     if (cache->block_size % 16 != 0) return KVATTN_ERR_UNSUPPORTED;
     if (num_chunks == 0 || total_q == 0) return KVATTN_OK;

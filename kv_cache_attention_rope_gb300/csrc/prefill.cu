@@ -59,26 +59,34 @@ namespace {
 
 constexpr int kBM = 128;      // query rows per tile (two tiles per CTA: A and B)
 constexpr int kBN = 128;      // keys per KV tile
-constexpr int kHD = 128;      // head dim
 constexpr int kPage = 16;     // tokens per TMA copy of one block
 constexpr int kThreads = 320; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax A, warps 6-9 softmax B
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-
-constexpr int kTileBytes = kBM * kHD * 2;  // 32 KB: a Q tile, a K stage or a V stage
-constexpr int kPanel = kTileBytes / 2;     // 16 KB: 128 rows x 64 columns (Q tiles)
-constexpr int kPageBytes = kPage * kHD * 2; // 4 KB: one 16-token page of K or V
-constexpr int kOffQ = 0;                   // Q_A, Q_B
-constexpr int kOffK = 2 * kTileBytes;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+constexpr int kPanel = kBM * 128;          // 16 KB: 128 rows x 64 columns (one 128-byte swizzle panel of Q)
 constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
-constexpr int kOffX = kOffBar + 256;  // softmax exchange: row maxima [2][2][128], row sums [2][2][128] (fp32)
-constexpr int kOffOrder = kOffX + 4096;  // work order: sorted pairs, tiles per pair (int32)
-constexpr int kMaxPairs = 1024;         // more (chunk, 256-row) pairs than this: unsorted order
-constexpr int kOffStage = (kOffOrder + 2 * kMaxPairs * 4 + 1023) / 1024 * 1024;  // output staging, 2 KB per softmax warp
-constexpr int kSmemBytes = kOffStage + 8 * 2048 + 1024;  // + slack to align the base to 1 KB
+constexpr int kMaxPairs = 1024;            // more (chunk, 256-row) pairs than this: unsorted order
 static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit before the exchange area");
+
+// Shared-memory geometry for head dim kD (64 or 128): a row of Q, K or V is
+// kD / 64 panels of 128 bytes; a K/V stage is [8-key group][panel][8 keys]
+// [128 B], so a 16-token page is one contiguous block of the stage.
+template <int kD>
+struct Geo {
+    static constexpr int kPanels = kD / 64;
+    static constexpr int kTileBytes = kBM * kD * 2;  // a Q tile, a K stage or a V stage (32 KB at D = 128)
+    static constexpr int kGroup = 8 * kD * 2;        // one 8-key group of a stage (all panels)
+    static constexpr int kPageBytes = kPage * kD * 2; // one 16-token page of K or V (4 KB at D = 128)
+    static constexpr int kOffQ = 0;                   // Q_A, Q_B
+    static constexpr int kOffK = 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+    static constexpr int kOffX = kOffBar + 256;  // softmax exchange: row maxima [2][2][128], row sums [2][2][128] (fp32)
+    static constexpr int kOffOrder = kOffX + 4096;  // work order: sorted pairs, tiles per pair (int32)
+    static constexpr int kOffStage = (kOffOrder + 2 * kMaxPairs * 4 + 1023) / 1024 * 1024;  // output staging, 2 KB per softmax warp
+    static constexpr int kSmemBytes = kOffStage + 8 * 2048 + 1024;  // + slack to align the base to 1 KB
+    static_assert(kD == 64 || kD == 128, "head dim");
+};
 
 struct Maps {
     CUtensorMap q;  // 3-D: (D, Hq, total_q), box (64, 1, 128)
@@ -214,12 +222,16 @@ __device__ __forceinline__ Item make_item(const PrefillArgs& a, int n_qt, int pa
 // ones without a global counter.  Pipeline state (stages, phases) runs on
 // across items, so the next item's Q, K, V and first S overlap the current
 // item's last tiles and epilogue.
+template <int kHD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ Maps maps, const int n_qt)
 {
+    using GE = Geo<kHD>;
+    constexpr int kTileBytes = GE::kTileBytes, kPageBytes = GE::kPageBytes, kGroup = GE::kGroup;
+    constexpr int kOffQ = GE::kOffQ, kOffK = GE::kOffK, kOffV = GE::kOffV;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + GE::kOffBar);
     Bars B;
     {
         uint64_t* b = bar;
@@ -236,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* order = reinterpret_cast<int*>(smem + kOffOrder);  // sorted pairs
+    int* order = reinterpret_cast<int*>(smem + GE::kOffOrder);  // sorted pairs
     int* plen = order + kMaxPairs;                          // tiles per pair
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -316,12 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 go = ii > 0 ? wait_or_abort(B.q_empty, (ii - 1) & 1, abort_flag, a.status) : !*abort_flag;
                 if (go) {
                     mbar_arrive_expect_tx(B.q_full, 2 * kTileBytes);
-                    for (int x = 0; x < 2; ++x) {
-                        tma_load_3d(smem + kOffQ + x * kTileBytes, &maps.q, 0, it.j, it.row0 + x * kBM, B.q_full,
-                                    pol_q);
-                        tma_load_3d(smem + kOffQ + x * kTileBytes + kPanel, &maps.q, 64, it.j, it.row0 + x * kBM,
-                                    B.q_full, pol_q);
-                    }
+                    for (int x = 0; x < 2; ++x)
+                        for (int p = 0; p < GE::kPanels; ++p)
+                            tma_load_3d(smem + kOffQ + x * kTileBytes + p * kPanel, &maps.q, 64 * p, it.j,
+                                        it.row0 + x * kBM, B.q_full, pol_q);
                 }
             }
             go = __shfl_sync(0xffffffffu, go, 0);
@@ -359,9 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 go = __shfl_sync(0xffffffffu, go, 0);
                 if (!go) break;
-                if (have)
-                    tma_load_4d(smem + kOffK + ks * kTileBytes + lane * kPageBytes, &maps.k, 0, 0, 0, y >> 3,
-                                &B.k_full[ks], pol_kv);
+                if (have) {
+                    if constexpr (kHD == 128)
+                        tma_load_4d(smem + kOffK + ks * kTileBytes + lane * kPageBytes, &maps.k, 0, 0, 0, y >> 3,
+                                    &B.k_full[ks], pol_kv);
+                    else
+                        tma_load_2d(smem + kOffK + ks * kTileBytes + lane * kPageBytes, &maps.k, 0, y, &B.k_full[ks],
+                                    pol_kv);
+                }
                 kg = g + 1;
                 // V stage g % kVStages: free once PV_A and PV_B of tile g - kVStages are done
                 const int vs = g % kVStages;
@@ -372,9 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 go = __shfl_sync(0xffffffffu, go, 0);
                 if (!go) break;
-                if (have)
-                    tma_load_4d(smem + kOffV + vs * kTileBytes + lane * kPageBytes, &maps.v, 0, 0, 0, y >> 3,
-                                &B.v_full[vs], pol_kv);
+                if (have) {
+                    if constexpr (kHD == 128)
+                        tma_load_4d(smem + kOffV + vs * kTileBytes + lane * kPageBytes, &maps.v, 0, 0, 0, y >> 3,
+                                    &B.v_full[vs], pol_kv);
+                    else
+                        tma_load_2d(smem + kOffV + vs * kTileBytes + lane * kPageBytes, &maps.v, 0, y, &B.v_full[vs],
+                                    pol_kv);
+                }
                 vg = g + 1;
             }
         }
@@ -399,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kHD, true);
         const uint32_t sbase = smem_addr(smem);
         const uint64_t dQ = umma_desc_sw128(sbase + kOffQ, 16, 1024);    // Q_x: + x * kTileBytes
-        const uint64_t dK = umma_desc_sw128(sbase + kOffK, 16, 2048);    // K stage s: + s * kTileBytes
-        const uint64_t dV = umma_desc_sw128(sbase + kOffV, 1024, 2048);  // V stage s: + s * kTileBytes
+        const uint64_t dK = umma_desc_sw128(sbase + kOffK, 16, kGroup);    // K stage s: + s * kTileBytes
+        const uint64_t dV = umma_desc_sw128(sbase + kOffV, 1024, kGroup);  // V stage s: + s * kTileBytes
         constexpr uint64_t kTileStep = kTileBytes >> 4;
         auto issue_s = [&](int x, int g) {  // S_x = Q_x K_g^T
             if (elect_one()) {
@@ -423,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)  // k-step: 16 keys = two 8-key groups
-                    tc_mma_f16_ts(d, pa + k * 8, vd + (uint64_t)((k * 2 * 2048) >> 4), idesc_o, (!first || k > 0));
+                    tc_mma_f16_ts(d, pa + k * 8, vd + (uint64_t)((k * 2 * kGroup) >> 4), idesc_o, (!first || k > 0));
                 if (x == 1) tc_commit(&B.v_empty[g % kVStages]);
                 if (last) tc_commit(&B.o_done[x]);
             }
@@ -490,8 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;        // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        float* xchg = reinterpret_cast<float*>(smem + kOffX);  // [2 tile phases][2 halves][128 rows]
-        unsigned char* stage = smem + kOffStage + (warp - 2) * 2048;  // this warp's output staging tile
+        float* xchg = reinterpret_cast<float*>(smem + GE::kOffX);  // [2 tile phases][2 halves][128 rows]
+        unsigned char* stage = smem + GE::kOffStage + (warp - 2) * 2048;  // this warp's output staging tile
         const float sl2 = a.scale_log2;
         int g = 0, ii = 0;
         bool ok = true;
@@ -505,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     const uint32_t tS = tmem + lane_base + x * 128 + hf * 64;
-                    const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * 64;
+                    const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * (kHD / 2);
                     const int pos_r = it.pos0 + x * kBM + r;  // absolute position of this row
                     const int pos_first = it.pos0 + x * kBM;  // ... of the tile's first row
                     // keys past the end of the sequence: V rows must be zero (stale
@@ -583,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the others)
                     if (__any_sync(0xffffffffu, rescale && t > 0)) {
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
+                        for (int q = 0; q < kHD / 64; ++q) {
                             uint32_t v[32];
                             tmem_ld32(tO + q * 32, v);
                             tmem_ld_wait();
@@ -594,10 +614,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (zero_v) {
                         if (t * kBN + r >= it.seq_len) {
-                            unsigned char* vrow = smem + kOffV + (g % kVStages) * kTileBytes + (r >> 3) * 2048 +
-                                                  hf * 1024 + (r & 7) * 128;
+                            // key r's row of the V stage: this half zeroes its kHD bytes
+                            unsigned char* vrow = smem + kOffV + (g % kVStages) * kTileBytes + (r >> 3) * kGroup +
+                                                  (r & 7) * 128 + hf * (kHD == 128 ? 1024 : 64);
 #pragma unroll
-                            for (int ch = 0; ch < 8; ++ch)
+                            for (int ch = 0; ch < kHD / 16; ++ch)
                                 *reinterpret_cast<uint4*>(vrow + ch * 16) = make_uint4(0, 0, 0, 0);
                         }
                         fence_async_smem();
@@ -609,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // epilogue: O / l -> bf16 rows of out, half hf writing columns
-            // 64hf..64hf+63.  The O reads complete before this item's last
+            // hf kHD/2 .. (hf + 1) kHD/2 - 1.  The O reads complete before this item's last
             // arrivals are followed by the next item's first P, which is what
             // lets the next item's first P.V overwrite O.
             const bool good = warp_wait(&B.o_done[0], ii & 1, abort_flag, a.status) &&
@@ -628,14 +649,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float l = lsum[x] + lx[((1 - hf) * 2 + x) * 128 + r];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 const int row = x * kBM + r;  // row of the 256
-                const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * 64;
+                const uint32_t tO = tmem + lane_base + 256 + x * 128 + hf * (kHD / 2);
                 // this warp's 32 rows all belong to the item: TMA store of a
                 // 32-row x 32-column box per chunk from a 64-byte-swizzled
                 // staging tile (rows past the item's end belong to other
                 // chunks and are never written: plain stores there)
                 const bool full = x * kBM + quarter * 32 + 32 <= it.rows;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < kHD / 64; ++q) {
                     uint32_t v[32];
                     tmem_ld32(tO + q * 32, v);
                     tmem_ld_wait();
@@ -654,12 +675,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fence_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_3d(&maps.o, hf * 64 + q * 32, it.j, it.row0 + x * kBM + quarter * 32, stage);
+                            tma_store_3d(&maps.o, hf * (kHD / 2) + q * 32, it.j, it.row0 + x * kBM + quarter * 32, stage);
                             bulk_commit_group();
                         }
                     } else if (row < it.rows) {
                         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                              ((int64_t)(it.row0 + row) * a.hq + it.j) * kHD + hf * 64 + q * 32;
+                                              ((int64_t)(it.row0 + row) * a.hq + it.j) * kHD + hf * (kHD / 2) + q * 32;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
                             *reinterpret_cast<uint4*>(orow + 8 * c) =
@@ -702,6 +723,7 @@ EncodeTiled encoder()
     return fn;
 }
 
+template <int kHD>
 bool make_maps(const PrefillArgs& a, Maps& m)
 {
     EncodeTiled enc = encoder();
@@ -722,7 +744,22 @@ bool make_maps(const PrefillArgs& a, Maps& m)
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
-    return pool_maps(a.k_pool, a.v_pool, (int64_t)a.num_blocks * a.hkv * a.block_size, false, &m.k, &m.v);
+    const int64_t rows = (int64_t)a.num_blocks * a.hkv * a.block_size;
+    if constexpr (kHD == 128) {
+        return pool_maps(a.k_pool, a.v_pool, rows, false, &m.k, &m.v);
+    } else {
+        // (64 columns, rows): a box of (64, 16) is one 16-row page, [16 rows][128 B]
+        const cuuint64_t pdims[2] = {64, (cuuint64_t)rows};
+        const cuuint64_t pstrides[1] = {64 * 2};
+        const cuuint32_t pbox[2] = {64, 16};
+        const cuuint32_t pestr[2] = {1, 1};
+        for (int i = 0; i < 2; ++i)
+            if (enc(i ? &m.v : &m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(i ? a.v_pool : a.k_pool),
+                    pdims, pstrides, pbox, pestr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return false;
+        return true;
+    }
 }
 
 }  // namespace
@@ -732,8 +769,8 @@ bool make_row_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtenso
     EncodeTiled enc = encoder();
     if (!enc || rows <= 0) return false;
     // (128 columns, rows): a box of (64, 16) is one 64-column panel of 16 rows
-    const cuuint64_t dims[2] = {(cuuint64_t)kHD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kHD * 2};
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128 * 2};
     const cuuint32_t box[2] = {64, 16};
     const cuuint32_t estr[2] = {1, 1};
     for (int i = 0; i < 2; ++i)
@@ -751,7 +788,7 @@ bool make_page_maps(const void* k_pool, const void* v_pool, int64_t rows, CUtens
     // (64 columns, 8 rows, 2 panels, rows / 8): a box of (64, 8, 2, 2) is one
     // 16-row page, landing as [8-row group][64-column panel][row][128 B]
     const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)rows / 8};
-    const cuuint64_t strides[3] = {(cuuint64_t)kHD * 2, 128, (cuuint64_t)kHD * 2 * 8};
+    const cuuint64_t strides[3] = {128 * 2, 128, 128 * 2 * 8};
     const cuuint32_t box[4] = {64, 8, 2, 2};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     for (int i = 0; i < 2; ++i)
@@ -800,22 +837,34 @@ bool pool_maps(const void* k_pool, const void* v_pool, int64_t rows, bool row_bo
     return true;
 }
 
-kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
+namespace {
+
+template <int kHD>
+kvattn_status launch_prefill_d(const PrefillArgs& a, cudaStream_t s)
 {
-    if (a.d != kHD || a.hq % a.hkv) return KVATTN_ERR_UNSUPPORTED;
     if ((int64_t)a.num_blocks * a.hkv * a.block_size >= ((int64_t)1 << 31)) return KVATTN_ERR_UNSUPPORTED;
     Maps maps;
-    if (!make_maps(a, maps)) return KVATTN_ERR_CUDA;
+    if (!make_maps<kHD>(a, maps)) return KVATTN_ERR_CUDA;
+    constexpr int kSmem = Geo<kHD>::kSmemBytes;
     static SmemLimit limit;
-    if (limit.ensure(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes) != cudaSuccess)
-        return KVATTN_ERR_CUDA;
+    if (limit.ensure(reinterpret_cast<const void*>(prefill_kernel<kHD>), kSmem) != cudaSuccess) return KVATTN_ERR_CUDA;
     const int n_qt = (a.max_q_len + 2 * kBM - 1) / (2 * kBM);
     const int64_t items = (int64_t)a.num_chunks * n_qt * a.hq;
     if (items <= 0) return KVATTN_OK;
     if (items > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
     const int64_t grid = std::min<int64_t>(items, num_sms());  // persistent: one CTA per SM
-    prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, maps, n_qt);
+    prefill_kernel<kHD><<<(unsigned)grid, kThreads, kSmem, s>>>(a, maps, n_qt);
     return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s)
+{
+    if (a.hq % a.hkv) return KVATTN_ERR_UNSUPPORTED;
+    if (a.d == 128) return launch_prefill_d<128>(a, s);
+    if (a.d == 64) return launch_prefill_d<64>(a, s);
+    return KVATTN_ERR_UNSUPPORTED;
 }
 
 }  // namespace kvattn

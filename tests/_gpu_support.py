@@ -165,8 +165,8 @@ class PrefillCase:
     tokens before each prefix are drawn N(0,1) and written to both caches."""
 
     def __init__(self, hq, hkv, prefixes, qlens, block_size=16, seed=0, device="cuda", k_scale=None,
-                 extra_blocks=5):
-        D = 128
+                 extra_blocks=5, head_dim=128):
+        D = head_dim
         self.hq, self.hkv, self.D = hq, hkv, D
         self.prefixes = np.asarray(prefixes, dtype=np.int64)
         self.qlens = np.asarray(qlens, dtype=np.int64)

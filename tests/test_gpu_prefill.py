@@ -90,3 +90,23 @@ def test_unsorted_schedule_many_chunks(kvattn_lib):
     case = PrefillCase(4, 1, prefixes, [1] * n, seed=7)
     rows = np.arange(0, n, 11)
     _check(kvattn_lib, case, rows=rows, what="unsorted schedule")
+
+
+@pytest.mark.parametrize("hq,hkv,block_size", [(12, 12, 16), (16, 4, 16), (12, 12, 1040)])
+def test_head_dim_64_gpt2_shape(kvattn_lib, hq, hkv, block_size):
+    """Head dim 64 (GPT-2: 12 heads x 64, and a grouped variant): chunks over
+    prefixes drawn like the GPT-2-shape decode workload (past U[1, 1024]), on a
+    paged cache of 16-token blocks and on one of 1040-token blocks (the
+    contiguous layout's row size rounded to a multiple of 16)."""
+    g = np.random.default_rng(64 + hkv)
+    prefixes = [int(p) for p in g.integers(1, 1025, 6)]
+    qlens = [130, 1, 64, 257, 17, 16]
+    case = PrefillCase(hq, hkv, prefixes, qlens, block_size=block_size, seed=64, head_dim=64,
+                       extra_blocks=5 if block_size == 16 else 1)
+    rows = np.arange(0, int(sum(qlens)), 3)
+    _check(kvattn_lib, case, rows=rows, what=f"D=64 {hq}/{hkv} BS {block_size}")
+
+
+def test_head_dim_64_full_chunk_no_prefix(kvattn_lib):
+    """A whole 512-token GPT-2 prompt as one chunk (prefix 0), every row checked."""
+    _check(kvattn_lib, PrefillCase(12, 12, [0], [512], seed=65, head_dim=64), what="D=64 prompt")

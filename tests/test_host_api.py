@@ -268,7 +268,8 @@ def test_prefill_validation(kv):
 
     cfg = kv.make_config(32, 8, 128, kv.BF16)
     assert call(kv.make_config(32, 8, 128, kv.F32), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]
-    assert call(kv.make_config(32, 8, 64, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert call(kv.make_config(32, 8, 80, kv.BF16), _cache(kv)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert call(kv.make_config(12, 12, 64, kv.BF16), _cache(kv), n=0) == E["KVATTN_OK"]   # GPT-2 shape accepted
     assert call(cfg, _cache(kv), n=-1) == E["KVATTN_ERR_INVALID_ARG"]
     assert call(cfg, _cache(kv), n=0) == E["KVATTN_OK"]
     assert call(cfg, _cache(kv), out=None) == E["KVATTN_ERR_INVALID_ARG"]
