@@ -142,9 +142,11 @@ __host__ __device__ constexpr int stage_bytes() { return kFP8 ? kF8Page : Traits
 
 // Query heads a consumer warp merges per pass (its merge slot's size): a
 // GQA group of 8 on the tensor cores is merged in two passes of 4, which keeps
-// the slot, and with it the ring depth, as for groups of 4.
-template <int kGT>
-__host__ __device__ constexpr int merge_heads() { return kGT < 4 ? kGT : 4; }
+// the slot, and with it the ring depth, as for groups of 4.  The fp8 path
+// merges one head per pass: its 4 KB pages leave room for 12 ring stages at 4
+// CTAs per SM only with the smaller slot (8 stages with slots of 4 heads).
+template <int kGT, bool kFP8 = false>
+__host__ __device__ constexpr int merge_heads() { return kFP8 ? 1 : kGT < 4 ? kGT : 4; }
 
 template <bool kBF16, int kD, int kGT, bool kFP8 = false>
 __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
@@ -156,9 +158,10 @@ __host__ __device__ inline SharedLayout shared_layout(int stages, int batch)
     off += stages * stage_bytes<kBF16, kD, kGT, kFP8>();
     // per consumer warp: its merge slot (kGT x (D + 2) floats, written at the
     // end of a piece) doubles as its probability buffer while tiles stream
-    constexpr int kMG = merge_heads<kGT>();
-    static_assert(kMG == kGT || kGT > 4, "only groups above 4 are merged in passes");
-    static_assert(kGT > 4 || T::kTG * T::kV * 8 <= kMG * (kD + 2) * 4, "probability buffer fits the merge slot");
+    constexpr int kMG = merge_heads<kGT, kFP8>();
+    static_assert(kMG == kGT || kGT > 4 || kFP8, "only groups above 4 and fp8 pages are merged in passes");
+    static_assert(kGT > 4 || kFP8 || T::kTG * T::kV * 8 <= kMG * (kD + 2) * 4,
+                  "probability buffer fits the merge slot");
     L.merge_off = off;
     off += kConsumerWarps * kMG * (kD + 2) * 4;
     L.pbuf_off = L.merge_off;
@@ -359,12 +362,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
                 const int64_t blk = blk_next;
                 if (base + 32 < pc.t1) blk_next = fetch(base + 32 + lane);
                 const int cnt = min(32, pc.t1 - base);
-                for (int j = 0; j < cnt; ++j) {
-                    const int64_t bj = __shfl_sync(0xffffffffu, blk, j);
-                    if (lane == 0) {
-                        const uint32_t stage = pos % stages, use = pos / stages;
-                        bool go = !*abort_flag;
-                        if (go && use > 0) go = mbar_wait(&empty[stage], (use - 1) & 1, a.status);
+                // fp8 pages: kConsumerWarps tiles at a time, one per lane.  Their
+                // stages are consecutive, freed by the consumer warps' concurrent
+                // tiles, so the lanes' waits overlap and one instruction stream
+                // issues all of their 4 KB copies (one lane issuing them in turn
+                // could not keep HBM busy).  The 8 KB tiles of a bf16 cache go
+                // one at a time: their shallower ring (two stages per consumer
+                // warp) cannot afford a lane's copy waiting for its group's
+                // slowest stage.
+                constexpr int kIssue = kFP8 ? kConsumerWarps : 1;
+                for (int j0 = 0; j0 < cnt; j0 += kIssue) {
+                    const int j = j0 + lane;
+                    const int64_t bj = __shfl_sync(0xffffffffu, blk, j & 31);
+                    const bool aborted = *abort_flag != 0;
+                    if (lane < kIssue && j < cnt && !aborted) {
+                        const uint32_t my = pos + lane;
+                        const uint32_t stage = my % stages, use = my / stages;
+                        bool go = true;
+                        if (use > 0) go = mbar_wait(&empty[stage], (use - 1) & 1, a.status);
                         if (!go) {
                             *abort_flag = 1;
                         } else {
@@ -402,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
                             }
                         }
                     }
-                    ++pos;
+                    __syncwarp();
+                    pos += min(kIssue, cnt - j0);
                 }
             }
         }
@@ -419,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
     const int sub = lane % T::kLPG;      // lane inside the group
     const int M = T::mask(sub);          // XOR layout of this lane's partial scores
     const int hm = M / T::kTPG, tm = M % T::kTPG;
-    constexpr int kMG = merge_heads<kGT>();
+    constexpr int kMG = merge_heads<kGT, kFP8>();
     float2* pbuf = reinterpret_cast<float2*>(merge + (size_t)warp * kMG * (kD + 2)) + grp * T::kV;
     const int hq = a.hq;
     uint32_t pos = 0;
@@ -472,33 +488,41 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
         };
         if constexpr (kFP8) {
             // ---- fp8 pages on the tensor cores (f16 operands; e4m3 codes are
-            // exact in f16).  S = Q K^T: MMA 0 takes tokens {4i, 4i+1} and
-            // MMA 1 tokens {4i+2, 4i+3} as its columns, so that lane q4 ends
-            // with the scores of tokens 4q4 .. 4q4+3; the dims of each 16-wide
-            // k-step are permuted so that a lane's four K values are one
-            // 32-bit word.  Q is scaled by 2^-4 into f16 range, the K scales
-            // multiply S per token.  O += P V with the same token order: one
-            // 32-bit word of the transposed V page holds a lane's four tokens
-            // of one dim.  P carries each token's V scale over a lazy
-            // reference vref (rescaled like the running max).
+            // exact in f16), tokens on the M axis and query heads on N, so
+            // that no MMA row is padding: S^T = K Q^T is one m16n8k16 per
+            // 16-dim step and O^T += V^T P^T one per 16 dims.  Row r of S^T
+            // is token pi(r) = 4(r%8 / 2) + 2(r / 8) + r%2 of the page: lane
+            // (g4, q4) then holds tokens rk0 = pi(g4) and rk1 = rk0 + 2, and
+            // the dims of each k-step are permuted so that a lane's four K
+            // values are one 32-bit word.  The C fragment of S^T, converted to
+            // f16 P, becomes the B fragment of P^T by one 8x8 transpose per
+            // half (movmatrix), which lands tokens 4q4 .. 4q4+3 of head g4 in
+            // lane (g4, q4): one 32-bit word of the transposed V page holds a
+            // lane's four tokens of one dim, the A operand of O^T += V^T P^T.
+            // Q is scaled by 2^-4 into f16 range, the K scales multiply S per
+            // token.  P carries each token's V scale over a lazy reference
+            // vref (rescaled like the running max).
             const int g4 = lane >> 2, q4 = lane & 3;
-            const int rk0 = (g4 >> 1) * 4 + (g4 & 1), rk1 = rk0 + 2;  // K rows of this lane's columns
-            uint32_t qa[kD / 16][2];  // dims 16kk + 4q4 .. 16kk + 4q4 + 3
+            const int rk0 = (g4 >> 1) * 4 + (g4 & 1), rk1 = rk0 + 2;  // K rows (tokens) of this lane
+            uint32_t qb[kD / 16][2];  // B fragment: head g4, dims 16kk + 4q4 .. 16kk + 4q4 + 3
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
-                qa[kk][0] = qa[kk][1] = 0u;
+                qb[kk][0] = qb[kk][1] = 0u;
                 if (g4 < kGT) {
                     const uint2 w = *reinterpret_cast<const uint2*>(
                         reinterpret_cast<const __nv_bfloat16*>(a.q) + ((int64_t)pc.b * hq + qh0 + g4) * kD + kk * 16 +
                         4 * q4);
-                    qa[kk][0] = pack_f16_rn(bf16lo(w.x) * 0.0625f, bf16hi(w.x) * 0.0625f);
-                    qa[kk][1] = pack_f16_rn(bf16lo(w.y) * 0.0625f, bf16hi(w.y) * 0.0625f);
+                    qb[kk][0] = pack_f16_rn(bf16lo(w.x) * 0.0625f, bf16hi(w.x) * 0.0625f);
+                    qb[kk][1] = pack_f16_rn(bf16lo(w.y) * 0.0625f, bf16hi(w.y) * 0.0625f);
                 }
             }
-            float o[kD / 8][2];
+            // O^T fragments: dims 16m + g4 (o[m][0], o[m][1]) and 16m + 8 + g4
+            // (o[m][2], o[m][3]) of heads 2q4 (even entries) and 2q4 + 1 (odd)
+            float o[kD / 16][4];
 #pragma unroll
-            for (int nd = 0; nd < kD / 8; ++nd) o[nd][0] = o[nd][1] = 0.f;
-            float m_run = -INFINITY, lrun = 0.f, vref = 0.f, vinv = 0.f;
+            for (int m = 0; m < kD / 16; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};  // heads 2q4, 2q4 + 1
+            float vref = 0.f, vinv = 0.f;
             const float sl2 = a.scale_log2 * 16.f;  // undoes the 2^-4 on Q
             for (int li = 0; li < ntiles; ++li) {
                 const uint32_t p = pos + li;
@@ -514,85 +538,120 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
                 const unsigned char* pg = ring + (size_t)stage * kStageB;
                 const int tok0 = (pc.t0 + li) * kTile;
                 const int nvalid = min(kTile, pc.len - tok0);
-                float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+                float s[4] = {0.f, 0.f, 0.f, 0.f};  // S^T: (rk0, 2q4), (rk0, 2q4+1), (rk1, 2q4), (rk1, 2q4+1)
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t w0 =
                         *reinterpret_cast<const uint32_t*>(pg + rk0 * 128 + ((kk ^ f8_swz(rk0)) << 4) + 4 * q4);
                     const uint32_t w1 =
                         *reinterpret_cast<const uint32_t*>(pg + rk1 * 128 + ((kk ^ f8_swz(rk1)) << 4) + 4 * q4);
-                    mma_f16_16816_top(s0, qa[kk][0], qa[kk][1], e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16));
-                    mma_f16_16816_top(s1, qa[kk][0], qa[kk][1], e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w1 >> 16));
+                    mma_f16_16816(s, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
+                                  e4m3x2_to_f16x2(w1 >> 16), qb[kk][0], qb[kk][1]);
                 }
-                // row g4, tokens 4q4 + {0, 1} (s0) and 4q4 + {2, 3} (s1), in log2 units
-                const float4 ksc = *reinterpret_cast<const float4*>(pg + kF8KsOff + 16 * q4);
-                const float4 vsc4 = *reinterpret_cast<const float4*>(pg + kF8VsOff + 16 * q4);
-                float x[4] = {s0[0] * (ksc.x * sl2), s0[1] * (ksc.y * sl2), s1[0] * (ksc.z * sl2),
-                              s1[1] * (ksc.w * sl2)};
-                float sv[4] = {vsc4.x, vsc4.y, vsc4.z, vsc4.w};
+                // scores in log2 units
+                const float* ksc = reinterpret_cast<const float*>(pg + kF8KsOff);
+                const float* vsc = reinterpret_cast<const float*>(pg + kF8VsOff);
+                const float k0 = ksc[rk0] * sl2, k1 = ksc[rk1] * sl2;
+                float sv0 = vsc[rk0], sv1 = vsc[rk1];
+                float x[4] = {s[0] * k0, s[1] * k0, s[2] * k1, s[3] * k1};
                 uint32_t vmask = 0xffffffffu;  // bytes of this lane's V words that belong to valid tokens
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (4 * q4 + j >= nvalid) {
-                        x[j] = -INFINITY;
-                        sv[j] = 0.f;
-                        vmask &= ~(0xffu << (8 * j));
+                if (nvalid < kTile) {
+                    if (rk0 >= nvalid) {
+                        x[0] = x[1] = -INFINITY;
+                        sv0 = 0.f;
                     }
-                float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-                float vmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-                // lazy references: the max (raised when a tile exceeds it by
-                // more than 2^8) and the V scale (when a tile's is over 16x it)
-                float f = 1.f;
-                if (tmax > m_run + 8.f) {
-                    f = m_run == -INFINITY ? 0.f : fast_exp2(m_run - tmax);
-                    lrun *= f;
-                    m_run = tmax;
-                }
-                if (vmax > vref * 16.f) {
-                    if (vref > 0.f) f *= vref / vmax;
-                    vref = vmax;
-                    vinv = 1.f / vmax;
-                }
-                if (f != 1.f) {
+                    if (rk1 >= nvalid) {
+                        x[2] = x[3] = -INFINITY;
+                        sv1 = 0.f;
+                    }
 #pragma unroll
-                    for (int nd = 0; nd < kD / 8; ++nd) {
-                        o[nd][0] *= f;
-                        o[nd][1] *= f;
+                    for (int j = 0; j < 4; ++j)
+                        if (4 * q4 + j >= nvalid) vmask &= ~(0xffu << (8 * j));
+                }
+                // lazy references: the max of each head (raised when a tile
+                // exceeds it by more than 2^8) and the V scale (when a tile's
+                // is over 16x it); the tile's maxima over its 16 tokens are
+                // only formed when some lane's own values call for a raise
+                float l0 = fmaxf(x[0], x[2]), l1 = fmaxf(x[1], x[3]), lv = fmaxf(sv0, sv1);
+                const bool raise = l0 > m_run[0] + 8.f || l1 > m_run[1] + 8.f || lv > vref * 16.f;
+                if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                    for (int sh = 4; sh < 32; sh <<= 1) {
+                        l0 = fmaxf(l0, __shfl_xor_sync(0xffffffffu, l0, sh));
+                        l1 = fmaxf(l1, __shfl_xor_sync(0xffffffffu, l1, sh));
+                        lv = fmaxf(lv, __shfl_xor_sync(0xffffffffu, lv, sh));
+                    }
+                    float f0 = 1.f, f1 = 1.f;
+                    if (l0 > m_run[0] + 8.f) {
+                        f0 = m_run[0] == -INFINITY ? 0.f : fast_exp2(m_run[0] - l0);
+                        lrun[0] *= f0;
+                        m_run[0] = l0;
+                    }
+                    if (l1 > m_run[1] + 8.f) {
+                        f1 = m_run[1] == -INFINITY ? 0.f : fast_exp2(m_run[1] - l1);
+                        lrun[1] *= f1;
+                        m_run[1] = l1;
+                    }
+                    if (lv > vref * 16.f) {
+                        if (vref > 0.f) {
+                            f0 *= vref / lv;
+                            f1 *= vref / lv;
+                        }
+                        vref = lv;
+                        vinv = 1.f / lv;
+                    }
+#pragma unroll
+                    for (int m = 0; m < kD / 16; ++m) {
+                        o[m][0] *= f0;
+                        o[m][1] *= f1;
+                        o[m][2] *= f0;
+                        o[m][3] *= f1;
                     }
                 }
-                const float p0 = fast_exp2(x[0] - m_run), p1 = fast_exp2(x[1] - m_run);
-                const float p2 = fast_exp2(x[2] - m_run), p3 = fast_exp2(x[3] - m_run);
-                lrun += (p0 + p1) + (p2 + p3);
-                const uint32_t pa0 = pack_f16_rn(p0 * (sv[0] * vinv), p1 * (sv[1] * vinv));
-                const uint32_t pa2 = pack_f16_rn(p2 * (sv[2] * vinv), p3 * (sv[3] * vinv));
-                // V^T words: dim 8 nd + g4, tokens 4q4 .. 4q4+3 (stale tokens zeroed: 0 * NaN)
+                const float p0 = fast_exp2(x[0] - m_run[0]), p1 = fast_exp2(x[1] - m_run[1]);
+                const float p2 = fast_exp2(x[2] - m_run[0]), p3 = fast_exp2(x[3] - m_run[1]);
+                lrun[0] += p0 + p2;
+                lrun[1] += p1 + p3;
+                const float c0 = sv0 * vinv, c1 = sv1 * vinv;
+                // P^T B fragment: head g4, tokens 4q4, 4q4+1 (pb0) and 4q4+2, 4q4+3 (pb1)
+                const uint32_t pb0 = movmatrix_trans(pack_f16_rn(p0 * c0, p1 * c0));
+                const uint32_t pb1 = movmatrix_trans(pack_f16_rn(p2 * c1, p3 * c1));
+                // V^T words: dims 16m + g4 and 16m + 8 + g4, tokens 4q4 .. 4q4+3
+                // (stale tokens zeroed: 0 * NaN)
                 const unsigned char* vt = pg + kF8VOff + g4 * 16 + 4 * q4;
 #pragma unroll
-                for (int nd = 0; nd < kD / 8; ++nd) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vt + nd * 128) & vmask;
-                    mma_f16_16816_top(o[nd], pa0, pa2, e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
+                for (int m = 0; m < kD / 16; ++m) {
+                    const uint32_t wa = *reinterpret_cast<const uint32_t*>(vt + m * 256) & vmask;
+                    const uint32_t wb = *reinterpret_cast<const uint32_t*>(vt + m * 256 + 128) & vmask;
+                    mma_f16_16816(o[m], e4m3x2_to_f16x2(wa), e4m3x2_to_f16x2(wb), e4m3x2_to_f16x2(wa >> 16),
+                                  e4m3x2_to_f16x2(wb >> 16), pb0, pb1);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
             }
             pos += ntiles;
-            lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
-            lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                lrun[0] += __shfl_xor_sync(0xffffffffu, lrun[0], sh);
+                lrun[1] += __shfl_xor_sync(0xffffffffu, lrun[1], sh);
+            }
             __syncwarp();
 #pragma unroll
             for (int h0 = 0; h0 < kGT; h0 += kMG) {
-                if (g4 >= h0 && g4 < h0 + kMG) {
-                    float* mr = mw + (g4 - h0) * (kD + 2);
 #pragma unroll
-                    for (int nd = 0; nd < kD / 8; ++nd)
-                        *reinterpret_cast<float2*>(mr + nd * 8 + 2 * q4) = make_float2(o[nd][0] * vref, o[nd][1] * vref);
-                    if (q4 == 0) {
-                        mr[kD] = m_run;
-                        mr[kD + 1] = lrun;
+                for (int e = 0; e < 2; ++e) {
+                    const int hd = 2 * q4 + e;
+                    if (hd >= h0 && hd < h0 + kMG && hd < kGT) {
+                        float* mr = mw + (hd - h0) * (kD + 2);
+#pragma unroll
+                        for (int m = 0; m < kD / 16; ++m) {
+                            mr[16 * m + g4] = o[m][e] * vref;
+                            mr[16 * m + 8 + g4] = o[m][2 + e] * vref;
+                        }
+                        if (g4 == 0) {
+                            mr[kD] = m_run[e];
+                            mr[kD + 1] = lrun[e];
+                        }
                     }
                 }
                 merge_pass(h0);

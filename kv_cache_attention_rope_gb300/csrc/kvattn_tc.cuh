@@ -129,6 +129,27 @@ __device__ __forceinline__ void mma_f16_16816_top(float (&d)[2], uint32_t a0, ui
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
 }
 
+// d (16x8 fp32) += A (16x16 f16) x B (16x8 f16); fragments as mma_bf16_16816
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one 32-bit pair per lane
+// (lane 4r + c: row r, columns 2c and 2c + 1): the C-fragment layout of one
+// 8-row half of an m16n8 accumulator becomes the B-fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 // two e4m3 codes (low byte = first) -> f16x2, exact
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
 {
