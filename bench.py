@@ -54,7 +54,7 @@ def parse_args():
                    help="run the step over L layers: one multi-layer cache, each layer's q/k/v taken as views "
                         "of its own fused QKV projection output, rotated q into a dense buffer")
     p.add_argument("--kv-dtype", choices=["model", "fp8"], default="model",
-                   help="fp8: e4m3 KV cache with a scale per (slot, head) (decode-only workloads)")
+                   help="fp8: e4m3 KV cache with a scale per (slot, head) (bf16 workloads, head_dim 128)")
     p.add_argument("--graph", action="store_true",
                    help="also time launch-bound small workloads as CUDA-graph replays of 50 steps (L2 warm) "
                         "and as single steps after an L2 flush")
@@ -204,9 +204,8 @@ class Step:
                 wl = dataclasses.replace(wl, chunks=nc)
                 self.wl = wl
             subset = list(range(nc)) + list(range(nc, nc + nd))
-        if self.fp8 and (wl.dtype != "bf16" or wl.head_dim != 128 or (wl.chunks and chunks != 0) or self.layers > 1):
-            raise SystemExit("--kv-dtype fp8: bf16 decode-only workloads with head_dim 128, one layer "
-                             "(use --chunks 0 on a mixed workload)")
+        if self.fp8 and (wl.dtype != "bf16" or wl.head_dim != 128 or self.layers > 1):
+            raise SystemExit("--kv-dtype fp8: bf16 workloads with head_dim 128, one layer")
         if wl.layout == "paged":
             if compact_pool:
                 probe = workloads.make_batch(wl, num_blocks=1 << 30, rows_subset=subset)
@@ -335,6 +334,12 @@ class Step:
         self.splits = kv.decode_num_splits(self.cfg, self.n_dec, self.max_len, 0) if self.n_dec else 0
         nws = kv.decode_workspace_size(self.cfg, max(1, self.n_dec), self.max_len, 0)
         self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=device)
+        # fp8 prefill: its bf16 copy of the chunks' blocks
+        self.pre_kv_tokens = int(np.sum(total[:nchunk]))
+        self.ws_pre = None
+        if self.fp8 and nchunk:
+            n = kv.prefill_fp8_workspace_size(self.cfg, BS, self.table_host.shape[1], nchunk, self.pre_kv_tokens)
+            self.ws_pre = torch.empty(n, dtype=torch.uint8, device=device)
         self.h_out = torch.empty(self.out_dec.shape, dtype=dt).pin_memory()
         self.h_out_pre = torch.empty(self.out_pre.shape, dtype=dt).pin_memory()
         # algorithmic bytes / flops
@@ -344,6 +349,8 @@ class Step:
         if self.fp8:
             self.kv_bytes_decode = int(np.sum(total[nchunk:])) * 2 * H * (D + 4)
         self.kv_bytes_prefill = Lr * workloads.kv_bytes_read(wl, total[:nchunk])
+        if self.fp8:
+            self.kv_bytes_prefill = int(np.sum(total[:nchunk])) * 2 * H * (D + 4)
         self.rope_bytes = Lr * self.n_tok * 2 * (wl.num_q_heads + 2 * H) * D * E
         pre_flops = 0
         for c in range(nchunk):
@@ -351,7 +358,7 @@ class Step:
             pre_flops += 4 * D * wl.num_q_heads * int(np.sum(P + np.arange(n) + 1))
         self.prefill_flops = Lr * pre_flops
         self.launches_per_step = Lr * (1 + (1 if self.n_dec else 0) + (1 if self.splits > 1 else 0) +
-                                       (1 if nchunk else 0))
+                                       ((3 if self.fp8 else 1) if nchunk else 0))
 
     # host block allocator: hand out the blocks this step's tokens open, return them after
     def alloc_begin(self):
@@ -364,6 +371,13 @@ class Step:
     def alloc_end(self, ids):
         if ids is not None:
             self.alloc.free(ids[::-1])
+
+    def _prefill(self, cache, q, cu, prefix, table, out):
+        if self.fp8:
+            self.kv.prefill_chunk_fp8(self.cfg, cache, q, cu, prefix, table, self.max_q, self.pre_kv_tokens, out=out,
+                                      workspace=self.ws_pre)
+        else:
+            self.kv.prefill_chunk(self.cfg, cache, q, cu, prefix, table, self.max_q, out=out)
 
     def launch(self, ev=None):
         """One step: per layer rope_append, prefill_chunk, decode.  ev: per layer
@@ -384,8 +398,7 @@ class Step:
             if e is not None:
                 e[1].record()
             if self.nchunk:
-                kv.prefill_chunk(self.cfg, cache, self.q_pre, self.cu, self.prefix, self.d_table_pre, self.max_q,
-                                 out=self.out_pre)
+                self._prefill(cache, self.q_pre, self.cu, self.prefix, self.d_table_pre, self.out_pre)
             if e is not None:
                 e[2].record()
             if self.n_dec:
@@ -450,8 +463,7 @@ class Step:
             (kv.rope_append_fp8 if self.fp8 else kv.rope_append)(self.cfg, self.cache, d["q"], d["k"], d["v"],
                                                                   d["pos"], d["sid"], d["table"])
             if self.nchunk:
-                kv.prefill_chunk(self.cfg, self.cache, d["q_pre"], d["cu"], d["prefix"], d["table_pre"],
-                                 self.max_q, out=d["out_pre"])
+                self._prefill(self.cache, d["q_pre"], d["cu"], d["prefix"], d["table_pre"], d["out_pre"])
             if self.n_dec:
                 (kv.decode_fp8 if self.fp8 else kv.decode)(self.cfg, self.cache, d["q_dec"], d["table_dec"],
                                                             d["lens"], self.max_len, out=d["out_dec"],
@@ -613,13 +625,13 @@ def per_config(dev, steps: int, warmup: int, hbm: float, bf16_burst: float, peak
     split + combine time, KV GB/s and fraction of the measured HBM peak; c4 on
     its 180e9-byte pool, halved until it fits, the size used recorded), c4 over
     an fp8 cache, c4 with groups of 8 query heads (the same KV bytes), the
-    launch-bound GPT-2-shape configs as CUDA-graph replays, and the mixed step
-    over 32 layers."""
+    launch-bound GPT-2-shape configs as CUDA-graph replays, the mixed step
+    over an fp8 cache, and the mixed step over 32 layers."""
     import torch
 
     res = {}
-    plan = [("c3", {}), ("c4", {}), ("c4g8", {}), ("c4_fp8", {"kv_fp8": True}), ("c1_graph", {}), ("c2_graph", {}),
-            ("c5_32layers", {"layers": 32})]
+    plan = [("c3", {}), ("c4", {}), ("c4g8", {}), ("c4_fp8", {"kv_fp8": True}), ("c5_fp8", {"kv_fp8": True}),
+            ("c1_graph", {}), ("c2_graph", {}), ("c5_32layers", {"layers": 32})]
     for name, kw in plan:
         key = name.split("_")[0]
         wl = workloads.WORKLOADS[key]
@@ -727,9 +739,10 @@ def run_ours(args, rank, world):
     def roof_of(k):
         if k == "prefill":
             ach = st.prefill_flops / t_pre / 1e12
-            return {"kernel": "prefill_chunk", "bound": "tensor", "achieved": ach, "peak": bf16_peak,
+            kname = "prefill_fp8_plan+prefill_fp8_expand+prefill_chunk" if st.fp8 else "prefill_chunk"
+            return {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": bf16_peak,
                     "unit": "TFLOP/s", "frac": ach / bf16_peak,
-                    "traffic": measured_traffic("prefill_chunk", wl.key),
+                    "traffic": None if st.fp8 else measured_traffic("prefill_chunk", wl.key),
                     "peak_source": bf16_src}
         name = "decode_split+decode_combine" if k == "decode" else "rope_append"
         by = st.kv_bytes_decode if k == "decode" else st.rope_bytes

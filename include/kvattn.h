@@ -377,6 +377,47 @@ kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache*
                                    int32_t max_q_len, int32_t total_q, void* out, void* stream);
 
 /*
+ * kvattn_prefill_chunk_fp8 -- kvattn_prefill_chunk over a kvattn_cache_fp8:
+ * the same chunks, rows and causal rule, with K and V the dequantised values
+ * code * scale rounded to fp32 and then to bf16 (both to nearest even; within
+ * half a bf16 ulp plus half an fp32 ulp of code * scale).  [RoPE page],
+ * section 2 (the cache compressed to 8 bits); [Engine page], sections 3.3
+ * and 3.4.
+ *
+ * The chunks' pages are first expanded into such a bf16 copy in `workspace`,
+ * then the bf16 tensor-core prefill runs over that copy (the compute type of
+ * kvattn_prefill_chunk; kvattn_decode_fp8 instead keeps code * scale exact,
+ * the codes in f16 and the scales in fp32).
+ * cfg->dtype must be KVATTN_BF16 (q and out bf16), head_dim 128, block_size
+ * a multiple of 16 (else UNSUPPORTED / INVALID_ARG).
+ *
+ *   max_kv_tokens  host upper bound of the sum over chunks of
+ *                  prefix_lens[c] + (cu_q_lens[c+1] - cu_q_lens[c]); the copy
+ *                  holds ceil(max_kv_tokens / block_size) + num_chunks blocks.
+ *                  A step whose chunks need more blocks records BAD_INDEX on
+ *                  the device and leaves the rows of the chunks past the copy
+ *                  unspecified.
+ *   workspace      device memory of at least
+ *                  kvattn_prefill_fp8_workspace_size(cfg, block_size,
+ *                  max_blocks_per_seq, num_chunks, max_kv_tokens) bytes (any
+ *                  alignment), owned by the caller, not read before the call
+ *                  and free again once the stream has passed it.
+ * Other arguments as kvattn_prefill_chunk.  Errors: INVALID_ARG,
+ * UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA; device: BAD_INDEX, TIMEOUT.
+ * num_chunks == 0 launches nothing.
+ */
+size_t kvattn_prefill_fp8_workspace_size(const kvattn_config* cfg, int32_t block_size,
+                                         int32_t max_blocks_per_seq, int32_t num_chunks,
+                                         int64_t max_kv_tokens);
+kvattn_status kvattn_prefill_chunk_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache,
+                                       const void* q, const int32_t* cu_q_lens,
+                                       const int32_t* prefix_lens, const int32_t* block_table,
+                                       int32_t max_blocks_per_seq, int32_t num_chunks,
+                                       int32_t max_q_len, int32_t total_q, int64_t max_kv_tokens,
+                                       void* out, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
+/*
  * Waits for `stream`, then returns the device status word of the current
  * device in *out (KVATTN_OK if no kernel recorded an error since the last
  * read) and clears it.  Returns CUDA if the stream itself failed.

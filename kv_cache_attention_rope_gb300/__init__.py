@@ -35,6 +35,7 @@ EXPORTED = [
     "kvattn_version", "kvattn_status_string", "kvattn_rope_append", "kvattn_rope_append_strided",
     "kvattn_decode_workspace_size",
     "kvattn_decode_num_splits", "kvattn_decode", "kvattn_decode_static_scratch", "kvattn_prefill_chunk",
+    "kvattn_prefill_fp8_workspace_size", "kvattn_prefill_chunk_fp8",
     "kvattn_selftest_wait_timeout", "kvattn_get_device_status",
     "kvattn_allocator_create", "kvattn_allocator_destroy", "kvattn_alloc_blocks", "kvattn_free_blocks",
     "kvattn_share_blocks", "kvattn_claim_blocks", "kvattn_allocator_num_free", "kvattn_allocator_num_failures",
@@ -98,6 +99,9 @@ def _load():
         "kvattn_decode": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p, sz, p], ctypes.c_int),
         "kvattn_decode_static_scratch": ([cfgp, cachep, p, p, i32, p, i32, i32, i32, p, p], ctypes.c_int),
         "kvattn_prefill_chunk": ([cfgp, cachep, p, p, p, p, i32, i32, i32, i32, p, p], ctypes.c_int),
+        "kvattn_prefill_fp8_workspace_size": ([cfgp, i32, i32, i32, i64], sz),
+        "kvattn_prefill_chunk_fp8": ([cfgp, ctypes.POINTER(CacheFP8Desc), p, p, p, p, i32, i32, i32, i32, i64, p, p,
+                                      sz, p], ctypes.c_int),
         "kvattn_get_device_status": ([p, ctypes.POINTER(i32)], ctypes.c_int),
         "kvattn_selftest_wait_timeout": ([i32, p], ctypes.c_int),
         "kvattn_allocator_create": ([i64, ctypes.POINTER(p)], ctypes.c_int),
@@ -422,6 +426,34 @@ def prefill_chunk(cfg: Config, cache: Cache, q, cu_q_lens, prefix_lens, block_ta
                                    prefix_lens.shape[0], int(max_q_len), q.shape[0],
                                    _dev(out, "out", q.dtype), _stream(stream)),
           "kvattn_prefill_chunk")
+    return out
+
+
+def prefill_fp8_workspace_size(cfg: Config, block_size: int, max_blocks_per_seq: int, num_chunks: int,
+                               max_kv_tokens: int) -> int:
+    """kvattn_prefill_fp8_workspace_size (0 for invalid arguments)."""
+    return int(lib.kvattn_prefill_fp8_workspace_size(ctypes.byref(cfg), int(block_size), int(max_blocks_per_seq),
+                                                     int(num_chunks), int(max_kv_tokens)))
+
+
+def prefill_chunk_fp8(cfg: Config, cache: CacheFP8, q, cu_q_lens, prefix_lens, block_table, max_q_len: int,
+                      max_kv_tokens: int, out=None, workspace=None, stream=None):
+    """kvattn_prefill_chunk_fp8: causal attention of query chunks over an fp8 cache (bf16 q and output)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    n = prefix_lens.shape[0]
+    if workspace is None:
+        size = prefill_fp8_workspace_size(cfg, cache.desc.block_size, block_table.shape[1], n, max_kv_tokens)
+        workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=q.device)
+    check(lib.kvattn_prefill_chunk_fp8(ctypes.byref(cfg), ctypes.byref(cache.desc), _dev(q, "q", torch.bfloat16),
+                                       _dev(cu_q_lens, "cu_q_lens", torch.int32),
+                                       _dev(prefix_lens, "prefix_lens", torch.int32),
+                                       _dev(block_table, "block_table", torch.int32), block_table.shape[1], n,
+                                       int(max_q_len), q.shape[0], int(max_kv_tokens),
+                                       _dev(out, "out", torch.bfloat16), _dev(workspace, "workspace"),
+                                       workspace.numel(), _stream(stream)),
+          "kvattn_prefill_chunk_fp8")
     return out
 
 

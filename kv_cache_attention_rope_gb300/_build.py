@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvattn.so")
-SOURCES = ["api.cu", "rope_append.cu", "decode.cu", "decode_static.cu", "prefill.cu", "blocks.cu", "allocator.cpp"]
+SOURCES = ["api.cu", "rope_append.cu", "decode.cu", "decode_static.cu", "prefill.cu", "prefill_fp8.cu", "blocks.cu", "allocator.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

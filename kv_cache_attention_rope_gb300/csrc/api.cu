@@ -556,6 +556,56 @@ kvattn_status kvattn_prefill_chunk(const kvattn_config* cfg, const kvattn_cache*
     return launch_prefill(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t kvattn_prefill_fp8_workspace_size(const kvattn_config* cfg, int32_t block_size, int32_t max_blocks_per_seq,
+                                         int32_t num_chunks, int64_t max_kv_tokens)
+{
+    if (!config_ok(cfg) || config_supported(cfg) != KVATTN_OK) return 0;
+    if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128) return 0;
+    return fp8_prefill_layout(cfg->num_kv_heads, block_size, max_blocks_per_seq, num_chunks, max_kv_tokens).bytes;
+}
+
+kvattn_status kvattn_prefill_chunk_fp8(const kvattn_config* cfg, const kvattn_cache_fp8* cache, const void* q,
+                                       const int32_t* cu_q_lens, const int32_t* prefix_lens,
+                                       const int32_t* block_table, int32_t max_blocks_per_seq, int32_t num_chunks,
+                                       int32_t max_q_len, int32_t total_q, int64_t max_kv_tokens, void* out,
+                                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!config_ok(cfg) || num_chunks < 0 || max_q_len < 0 || total_q < 0 || max_kv_tokens < 0 || !cache)
+        return KVATTN_ERR_INVALID_ARG;
+    kvattn_status st = config_supported(cfg);
+    if (st != KVATTN_OK) return st;
+    if (cfg->dtype != KVATTN_BF16 || cfg->head_dim != 128) return KVATTN_ERR_UNSUPPORTED;
+    const kvattn_cache c{cache->pool, cache->pool, cache->num_blocks, cache->block_size};
+    if (!cache_ok(&c, max_blocks_per_seq) || cache->block_size % 16 != 0) return KVATTN_ERR_INVALID_ARG;
+    if (num_chunks == 0 || total_q == 0) return KVATTN_OK;
+    if (!q || !cu_q_lens || !prefix_lens || !block_table || !out || !workspace) return KVATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15u) return KVATTN_ERR_INVALID_ARG;
+    const Fp8PrefillLayout L =
+        fp8_prefill_layout(cfg->num_kv_heads, cache->block_size, max_blocks_per_seq, num_chunks, max_kv_tokens);
+    if (L.bytes == 0) return KVATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < L.bytes) return KVATTN_ERR_WORKSPACE_TOO_SMALL;
+    PrefillArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.cu_q_lens = cu_q_lens;
+    a.prefix_lens = prefix_lens;
+    a.block_table = block_table;
+    a.out = out;
+    a.num_blocks = cache->num_blocks;
+    a.block_size = cache->block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_chunks = num_chunks;
+    a.max_q_len = max_q_len;
+    a.total_q = total_q;
+    a.hq = cfg->num_q_heads;
+    a.hkv = cfg->num_kv_heads;
+    a.d = cfg->head_dim;
+    a.scale_log2 = scale_of(cfg) * 1.4426950408889634f;
+    a.status = device_status_ptr();
+    if (!a.status) return KVATTN_ERR_CUDA;
+    return launch_prefill_fp8(a, cache->pool, L, workspace, static_cast<cudaStream_t>(stream));
+}
+
 kvattn_status kvattn_selftest_wait_timeout(int32_t limit_us, void* stream)
 {
     if (limit_us < 1 || limit_us > 1000000) return KVATTN_ERR_INVALID_ARG;

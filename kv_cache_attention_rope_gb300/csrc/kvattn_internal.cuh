@@ -170,6 +170,20 @@ struct PrefillArgs {
 };
 kvattn_status launch_prefill(const PrefillArgs& a, cudaStream_t s);
 
+// Workspace of the fp8 prefill: the chunks' blocks expanded to bf16 (nb
+// blocks, K and V), their block table, owners and first blocks.  bytes == 0
+// for invalid arguments.
+struct Fp8PrefillLayout {
+    int64_t nb;
+    size_t off_first, off_owner, off_table, off_k, off_v, bytes;
+};
+Fp8PrefillLayout fp8_prefill_layout(int32_t hkv, int32_t block_size, int32_t max_blocks, int32_t num_chunks,
+                                    int64_t max_kv_tokens);
+// Expands the chunks' fp8 pages into the workspace, then runs launch_prefill
+// over the bf16 copy (pa's pools and table are replaced).
+kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const Fp8PrefillLayout& L,
+                                 void* workspace, cudaStream_t s);
+
 // ---------------------------------------------------------------- device side
 
 // First error wins; later ones are dropped.

@@ -396,21 +396,201 @@ __device__ __forceinline__ uint2 quant_row_fp8(const uint4& x, float& scale)
     return make_uint2(w[0], w[1]);
 }
 
-// This lane's 8 dims (8 * dv ..) of token r's K and V rows into their fp8
-// page (layout: kvattn_internal.cuh, kF8Page); lane dv == 0 writes the scales.
-__device__ __forceinline__ void put_page_fp8(unsigned char* page, int r, int dv, uint2 kc, float ks, uint2 vc,
-                                             float vs)
+// This lane's 8 dims (8 * dv ..) of token r's K row into its fp8 page
+// (layout: kvattn_internal.cuh, kF8Page); lane dv == 0 writes the scale.
+// V goes through append_v_fp8_kernel.
+__device__ __forceinline__ void put_k_page_fp8(unsigned char* page, int r, int dv, uint2 kc, float ks)
 {
     *reinterpret_cast<uint2*>(page + r * 128 + (((dv >> 1) ^ f8_swz(r)) << 4) + (dv & 1) * 8) = kc;
-    unsigned char* vt = page + kF8VOff + (dv * 8) * 16 + r;
+    if (dv == 0) reinterpret_cast<float*>(page + kF8KsOff)[r] = ks;
+}
+
+// V rows of an fp8 append.  The page stores V transposed (dim d's 16 tokens
+// in 16 consecutive bytes), so one token alone can only write single bytes,
+// 128 scattered partial-sector writes per head row, which made V the most
+// expensive part of a prefill chunk's append.  append_v_fp8_kernel groups
+// the tokens into runs of consecutive tokens that land in the same page (the
+// tokens of a chunk do, 16 at a time).  A CTA takes a window of 16 tokens;
+// one warp-wide scan of the window (and the tokens after it that a run may
+// reach) gives every run's start, length, slots and cache block.  A CTA is
+// one warp for one (window, KV head): many small CTAs keep every SM's memory
+// pipe busy and overlap the scans' latency.  Work items are each run of 2 or
+// more tokens and all single-token runs of the window together.  Lanes 2e
+// and 2e + 1 quantise token e's row (64 dims each, the row's amax agreed
+// with one shuffle) exactly as quant_row_fp8 does.  A run's codes go to a
+// shared-memory tile [slot][128 B] (16-byte chunks rotated by the slot,
+// conflict-free both ways); lane l then reads dims 4l .. 4l+3 of each group
+// of 4 slots, transposes the 4x4 bytes with byte permutes, and writes whole
+// 16-byte rows for a full page, 4-byte words for complete groups of 4 slots,
+// single bytes only at a run's ragged edges.  Single tokens (a decode step's)
+// write their bytes directly, 16 tokens per pass of the warp.
+constexpr int kVWin = 16;
+
+// Tokens share a page when they have the same sequence and position / 16
+// (the block table is per sequence); -1 for a token the append rejects.
+__device__ __forceinline__ long long page_id(const RopeArgs& a, int t, int& pos, int& blk)
+{
+    pos = a.positions[t];
+    const int seq = a.seq_ids[t];
+    if (pos < 0 || seq < 0 || seq >= a.num_seqs || pos / a.block_size >= a.max_blocks) return -1;
+    blk = a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size];
+    if (blk < 0 || blk >= a.num_blocks) return -1;  // recorded by the ring kernel
+    return (long long)seq * (((long long)a.max_blocks * a.block_size) / 16) + pos / 16;
+}
+
+// codes of 4 values (first in the low byte), e4m3 RN, saturating
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, float inv)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(a, inv), __fmul_rn(b, inv)), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(c, inv), __fmul_rn(d, inv)), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// Token t's head h row, this lane's half (dims 64 half ..): codes (chunk i =
+// 16 dims in w[i]) and the row's scale.  `pair` masks the lanes taking part.
+__device__ __forceinline__ void quant_half_row(const RopeArgs& a, int t, int h, int half, unsigned pair, uint4 (&w)[4],
+                                               float& scale)
+{
+    const uint4* src =
+        reinterpret_cast<const uint4*>((const char*)a.v + (int64_t)t * a.v_stride + ((int64_t)h * 128 + 64 * half) * 2);
+    uint4 x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = src[i];
+    float mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        mx[i] = fmaxf(fmaxf(fmaxf(fabsf(bf16lo(x[i].x)), fabsf(bf16hi(x[i].x))),
+                            fmaxf(fabsf(bf16lo(x[i].y)), fabsf(bf16hi(x[i].y)))),
+                      fmaxf(fmaxf(fabsf(bf16lo(x[i].z)), fabsf(bf16hi(x[i].z))),
+                            fmaxf(fabsf(bf16lo(x[i].w)), fabsf(bf16hi(x[i].w)))));
+    float amax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    amax = fmaxf(amax, __shfl_xor_sync(pair, amax, 1));
+    scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        vt[(2 * i) * 16] = (unsigned char)((i < 2 ? vc.x : vc.y) >> (16 * (i & 1)));
-        vt[(2 * i + 1) * 16] = (unsigned char)((i < 2 ? vc.x : vc.y) >> (16 * (i & 1) + 8));
+        const uint4 u0 = x[2 * i], u1 = x[2 * i + 1];
+        w[i].x = e4m3x4(bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), inv);
+        w[i].y = e4m3x4(bf16lo(u0.z), bf16hi(u0.z), bf16lo(u0.w), bf16hi(u0.w), inv);
+        w[i].z = e4m3x4(bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y), inv);
+        w[i].w = e4m3x4(bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w), inv);
     }
-    if (dv == 0) {
-        reinterpret_cast<float*>(page + kF8KsOff)[r] = ks;
-        reinterpret_cast<float*>(page + kF8VsOff)[r] = vs;
+}
+
+__device__ __forceinline__ unsigned char* fp8_page(const RopeArgs& a, int blk, int h, int pos)
+{
+    const int ppb = a.block_size / 16;
+    return (unsigned char*)a.k_pool + (((int64_t)blk * a.hkv + h) * ppb + (pos % a.block_size) / 16) * kF8Page;
+}
+
+__global__ void __launch_bounds__(32, 24) append_v_fp8_kernel(const __grid_constant__ RopeArgs a)
+{
+    __shared__ __align__(16) unsigned char tile[16 * 128];
+    __shared__ float tsc[16];
+    const int lane = threadIdx.x;
+    const int t0 = blockIdx.x * kVWin, h = blockIdx.y;
+    // scan: lane i holds token t0 - 1 + i (the token before the window, the
+    // window, and 15 tokens after it: a run starting in the window ends there)
+    const int u = t0 - 1 + lane;
+    int pos = 0, blk = 0;
+    const long long key = (u >= 0 && u < a.num_tokens) ? page_id(a, u, pos, blk) : -2;
+    const long long knext = __shfl_down_sync(0xffffffffu, key, 1);
+    const unsigned same_next = __ballot_sync(0xffffffffu, lane < 31 && key >= 0 && key == knext);
+    const long long kprev = __shfl_up_sync(0xffffffffu, key, 1);
+    const unsigned lead = __ballot_sync(0xffffffffu, lane >= 1 && lane <= kVWin && key >= 0 && key != kprev);
+    // run starting at lane b: lanes b .. b + n - 1, n = 1 + the set bits of same_next from bit b on (at most 16)
+    const int my_n = min(16, __ffs(~(same_next >> lane)));
+    const unsigned singles = lead & __ballot_sync(0xffffffffu, my_n == 1);
+    const unsigned multis = lead & ~singles;
+    const int nm = __popc(multis), items = nm + (singles ? 1 : 0);
+    const int e = lane >> 1, half = lane & 1;
+    for (int idx = 0; idx < items; ++idx) {
+        if (idx < nm) {
+            // ---- a run of n >= 2 tokens in one page
+            unsigned m = multis;
+            for (int k = idx; k > 0; --k) m &= m - 1;
+            const int b = __ffs(m) - 1;
+            const int n = __shfl_sync(0xffffffffu, my_n, b);
+            const int r = __shfl_sync(0xffffffffu, pos, min(b + e, 31)) & 15;  // slot of token e
+            const int blk_b = __shfl_sync(0xffffffffu, blk, b), pos_b = __shfl_sync(0xffffffffu, pos, b);
+            if (e < n) {
+                uint4 w[4];
+                float sc;
+                quant_half_row(a, t0 - 1 + b + e, h, half, 0xffffffffu >> (32 - 2 * n), w, sc);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(tile + r * 128 + 16 * ((4 * half + i) ^ (r & 7))) = w[i];
+                if (half == 0) tsc[r] = sc;
+            }
+            const uint32_t cov = __reduce_or_sync(0xffffffffu, e < n ? 1u << r : 0u);
+            __syncwarp();
+            // lane l: dims 4l .. 4l+3 (chunk l / 4 of every slot row, word l % 4)
+            const int c = lane >> 2, wo = 4 * (lane & 3);
+            uint32_t o[4][4];  // [dim k][slot group j]
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t x[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int rr = 4 * j + q;
+                    x[q] = *reinterpret_cast<const uint32_t*>(tile + rr * 128 + 16 * (c ^ (rr & 7)) + wo);
+                }
+                const uint32_t t01l = __byte_perm(x[0], x[1], 0x5140), t01h = __byte_perm(x[0], x[1], 0x7362);
+                const uint32_t t23l = __byte_perm(x[2], x[3], 0x5140), t23h = __byte_perm(x[2], x[3], 0x7362);
+                o[0][j] = __byte_perm(t01l, t23l, 0x5410);
+                o[1][j] = __byte_perm(t01l, t23l, 0x7632);
+                o[2][j] = __byte_perm(t01h, t23h, 0x5410);
+                o[3][j] = __byte_perm(t01h, t23h, 0x7632);
+            }
+            unsigned char* page = fp8_page(a, blk_b, h, pos_b);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                unsigned char* row = page + kF8VOff + 16 * (4 * lane + k);
+                if (cov == 0xffffu) {
+                    *reinterpret_cast<uint4*>(row) = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t q = (cov >> (4 * j)) & 15u;
+                        if (q == 15u) {
+                            *reinterpret_cast<uint32_t*>(row + 4 * j) = o[k][j];
+                        } else if (q) {
+#pragma unroll
+                            for (int bb = 0; bb < 4; ++bb)
+                                if (q >> bb & 1u) row[4 * j + bb] = (unsigned char)(o[k][j] >> (8 * bb));
+                        }
+                    }
+                }
+            }
+            if (lane < 16 && (cov >> lane & 1u)) reinterpret_cast<float*>(page + kF8VsOff)[lane] = tsc[lane];
+            __syncwarp();  // the tile is reused by the next run
+        } else {
+            // ---- the window's single-token runs, one per lane pair: bytes straight to their pages
+            const int ns = __popc(singles);
+            unsigned m = singles;
+            for (int k = min(e, 16); k > 0; --k) m &= m - 1;
+            const int b = m ? __ffs(m) - 1 : 0;
+            const int pb = __shfl_sync(0xffffffffu, pos, b), kb = __shfl_sync(0xffffffffu, blk, b);
+            if (e < ns) {
+                uint4 w[4];
+                float sc;
+                quant_half_row(a, t0 - 1 + b, h, half, 0xffffffffu >> (32 - 2 * ns), w, sc);
+                unsigned char* page = fp8_page(a, kb, h, pb);
+                unsigned char* col = page + kF8VOff + 16 * (64 * half) + (pb & 15);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t v4[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb)
+                            col[16 * (16 * i + 4 * q + bb)] = (unsigned char)(v4[q] >> (8 * bb));
+                }
+                if (half == 0) reinterpret_cast<float*>(page + kF8VsOff)[pb & 15] = sc;
+            }
+        }
     }
 }
 
@@ -480,10 +660,11 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
                     *abort_flag = 1;
                 } else {
                     unsigned char* dq = st + 16 + kTwBytes;
-                    mbar_arrive_expect_tx(&full[s], qbytes + 2 * kbytes);
+                    mbar_arrive_expect_tx(&full[s], qbytes + (kFP8 ? 1 : 2) * kbytes);  // fp8: V has its own kernel
                     bulk_load(dq, (const char*)a.q + t * a.q_stride, qbytes, &full[s], policy);
                     bulk_load(dq + qbytes, (const char*)a.k + t * a.k_stride, kbytes, &full[s], policy);
-                    bulk_load(dq + qbytes + kbytes, (const char*)a.v + t * a.v_stride, kbytes, &full[s], policy);
+                    if (!kFP8)
+                        bulk_load(dq + qbytes + kbytes, (const char*)a.v + t * a.v_stride, kbytes, &full[s], policy);
                 }
             }
             go = __shfl_sync(0xffffffffu, go, 0);
@@ -578,10 +759,9 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
                 const int64_t step = (int64_t)kGroups * pages * kF8Page;  // kGroups heads further
                 for (int u = 0; u < nk; ++u) {
                     const uint4 x = *reinterpret_cast<const uint4*>(ksrc + u * kHeadStep);
-                    float ks, vs;
+                    float ks;
                     const uint2 kc = quant_row_fp8<kVPH>(rotate16(x), ks);
-                    const uint2 vc = quant_row_fp8<kVPH>(*reinterpret_cast<const uint4*>(ksrc + kbytes + u * kHeadStep), vs);
-                    put_page_fp8(pg + u * step, h.off & 15, dv, kc, ks, vc, vs);
+                    put_k_page_fp8(pg + u * step, h.off & 15, dv, kc, ks);
                 }
             } else {
                 const int64_t slot =
@@ -662,7 +842,9 @@ kvattn_status launch_rope_append_fp8(const RopeArgs& a, cudaStream_t s)
     bool launched = false;
     if (a.dtype == KVATTN_BF16 && a.d == 128) launched = launch_pipe<true, 128, true>(a, s, err);
     if (!launched) return KVATTN_ERR_UNSUPPORTED;
-    return cuda_status(err);
+    if (err != cudaSuccess) return KVATTN_ERR_CUDA;
+    append_v_fp8_kernel<<<dim3((unsigned)((a.num_tokens + kVWin - 1) / kVWin), (unsigned)a.hkv), 32, 0, s>>>(a);
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace kvattn

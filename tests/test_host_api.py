@@ -275,6 +275,46 @@ def test_prefill_validation(kv):
     assert call(cfg, _cache(kv), out=None) == E["KVATTN_ERR_INVALID_ARG"]
 
 
+def test_prefill_fp8_validation_and_workspace(kv):
+    """kvattn_prefill_chunk_fp8's host checks and its workspace formula: a bf16
+    copy of ceil(max_kv_tokens / block_size) + num_chunks blocks (K and V),
+    the copy's block table, owners and first blocks, each part 1 KB aligned,
+    plus 1 KB of slack for the base alignment."""
+    E = kv.STATUS_CODE
+    cfg = kv.make_config(32, 8, 128, kv.BF16)
+
+    def size(config=cfg, bs=16, maxb=64, n=4, kvt=4096):
+        return kv.lib.kvattn_prefill_fp8_workspace_size(ctypes.byref(config), bs, maxb, n, kvt)
+
+    def call(c, config=cfg, n=2, kvt=1000, ws=FAKE, ws_bytes=1 << 40, out=FAKE):
+        return kv.lib.kvattn_prefill_chunk_fp8(ctypes.byref(config), ctypes.byref(c) if c is not None else None,
+                                               FAKE, FAKE, FAKE, FAKE, 64, n, 512, 1024, kvt, out, ws, ws_bytes,
+                                               None)
+
+    def up(x):
+        return -(-x // 1024) * 1024
+
+    nb = -(-4096 // 16) + 4
+    want = up(5 * 8) + up(nb * 4) + up(4 * 64 * 4) + 2 * up(nb * 8 * 16 * 128 * 2) + 1024
+    assert size() == want
+    assert size(config=kv.make_config(32, 8, 128, kv.F32)) == 0
+    assert size(config=kv.make_config(12, 12, 64, kv.BF16)) == 0
+    assert size(bs=24) == 0 and size(maxb=0) == 0 and size(n=-1) == 0 and size(kvt=-1) == 0
+    c8 = kv.CacheFP8Desc(FAKE, 8, 16)
+    assert call(None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(kv.CacheFP8Desc(None, 8, 16)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(kv.CacheFP8Desc(FAKE, 8, 24)) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(c8, config=kv.make_config(32, 8, 128, kv.F32)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert call(c8, config=kv.make_config(12, 12, 64, kv.BF16)) == E["KVATTN_ERR_UNSUPPORTED"]
+    assert call(c8, n=0) == E["KVATTN_OK"]
+    assert call(c8, n=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(c8, kvt=-1) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(c8, ws=None) == E["KVATTN_ERR_INVALID_ARG"]
+    assert call(c8, out=None) == E["KVATTN_ERR_INVALID_ARG"]
+    need = kv.lib.kvattn_prefill_fp8_workspace_size(ctypes.byref(cfg), 16, 64, 2, 1000)
+    assert call(c8, ws_bytes=need - 1) == E["KVATTN_ERR_WORKSPACE_TOO_SMALL"]
+
+
 def test_get_device_status_needs_out(kv):
     assert kv.lib.kvattn_get_device_status(None, None) == kv.STATUS_CODE["KVATTN_ERR_INVALID_ARG"]
 
