@@ -624,13 +624,13 @@ def per_config(dev, steps: int, warmup: int, hbm: float, bf16_burst: float, peak
     at a time (each freed before the next): the decode-only configs (decode
     split + combine time, KV GB/s and fraction of the measured HBM peak; c4 on
     its 180e9-byte pool, halved until it fits, the size used recorded), c4 over
-    an fp8 cache, c4 with groups of 8 query heads (the same KV bytes), the
+    an fp8 cache, c4 with groups of 8 and of 2 query heads (the same KV bytes), the
     launch-bound GPT-2-shape configs as CUDA-graph replays, the mixed step
     over an fp8 cache, and the mixed step over 32 layers."""
     import torch
 
     res = {}
-    plan = [("c3", {}), ("c4", {}), ("c4g8", {}), ("c4_fp8", {"kv_fp8": True}), ("c5_fp8", {"kv_fp8": True}),
+    plan = [("c3", {}), ("c4", {}), ("c4g8", {}), ("c4g2", {}), ("c4_fp8", {"kv_fp8": True}), ("c5_fp8", {"kv_fp8": True}),
             ("c1_graph", {}), ("c2_graph", {}), ("c5_32layers", {"layers": 32})]
     for name, kw in plan:
         key = name.split("_")[0]

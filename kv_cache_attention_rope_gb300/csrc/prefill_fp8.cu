@@ -284,7 +284,10 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
     prefill_fp8_plan<<<1, 1024, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
-    prefill_fp8_expand<<<num_sms() * 4, kExpandWarps * 32, 0, s>>>(a);
+    int per_sm = 0;  // one wave of resident CTAs (each warp walks a contiguous range of pages)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_fp8_expand, kExpandWarps * 32, 0);
+    if (e != cudaSuccess) return cuda_status(e);
+    prefill_fp8_expand<<<num_sms() * std::max(1, per_sm), kExpandWarps * 32, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
     PrefillArgs b = pa;

@@ -238,3 +238,16 @@ def test_c4_gqa8_full_size_sampled_rows(kvattn_lib):
     _check(case, out, "c4 GQA-8")
     del case
     torch.cuda.empty_cache()
+
+
+def test_c4_gqa2_full_size_sampled_rows(kvattn_lib):
+    """c4's lengths and block tables with 16 query heads over its 8 KV heads (groups of
+    2, the CUDA-core path) on a compact pool; 12 sampled rows."""
+    wl = workloads.WORKLOADS["c4g2"]
+    b = workloads.make_batch(wl, num_blocks=1 << 20)
+    case = DecodeCase(wl, b, list(range(0, 256, 22)), fill_nan=False)
+    _, out = case.run()
+    assert kvattn_lib.get_device_status() == 0
+    _check(case, out, "c4 GQA-2")
+    del case
+    torch.cuda.empty_cache()

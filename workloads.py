@@ -59,6 +59,10 @@ WORKLOADS = {
     "c4g8": Workload("c4g8", "GQA-8 decode bf16, batch 256, 64q/8kv x128, paged 16 over a 180e9-byte pool, "
                      "past len U[1024,8192]",
                      "bf16", 64, 8, 128, "paged", 16, 256, (1024, 8192), pool_bytes=180 * 10**9),
+    # c4 with groups of 2 query heads per KV head (the CUDA-core decode path): the same KV bytes as c4
+    "c4g2": Workload("c4g2", "GQA-2 decode bf16, batch 256, 16q/8kv x128, paged 16 over a 180e9-byte pool, "
+                     "past len U[1024,8192]",
+                     "bf16", 16, 8, 128, "paged", 16, 256, (1024, 8192), pool_bytes=180 * 10**9),
     "c5": Workload("c5", "mixed: 16 prefill chunks x 512 causal queries over prefix U[0,8192] + 128 decode "
                    "seqs past len U[256,8192], GQA 32q/8kv x128, paged 16",
                    "bf16", 32, 8, 128, "paged", 16, 128, (256, 8192),
