@@ -20,8 +20,10 @@
 //    block; and the copy's block table (chunk c, column j -> first[c] + j).
 //  - prefill_fp8_expand (persistent warps): one warp per 16-token page of
 //    one KV head.  Each warp takes a contiguous range of copy pages; its
-//    lanes look up 32 pages' sources at once, then the warp converts them one
-//    after another: K rows un-swizzled, V transposed back to token-major
+//    lanes look up 32 pages' sources at once, then the warp streams the pages
+//    through two shared-memory buffers (16-byte asynchronous copies of page
+//    i + 1 fly while page i converts) and converts them: K rows un-swizzled,
+//    V transposed back to token-major
 //    rows, every element written as bf16(code * scale) (the product in fp32,
 //    RN, then RN to bf16).  Only pages holding keys the prefill reads are
 //    converted; the prefill zeroes stale V rows of a sequence's last page
@@ -139,7 +141,9 @@ constexpr int kExpandWarps = 8;
 
 __global__ void __launch_bounds__(kExpandWarps * 32) prefill_fp8_expand(const Fp8PrefillArgs a)
 {
+    extern __shared__ __align__(16) unsigned char bufs[];  // [kExpandWarps][2][kF8Page]
     const int lane = threadIdx.x & 31;
+    unsigned char* pbuf = bufs + (threadIdx.x >> 5) * 2 * kF8Page;
     const int ppb = a.block_size / 16;  // pages per block and head
     const int64_t used = min(a.first[a.num_chunks], a.nb);
     const int64_t pages = used * a.hkv * ppb;
@@ -165,26 +169,52 @@ __global__ void __launch_bounds__(kExpandWarps * 32) prefill_fp8_expand(const Fp
                     my_src = a.pool + (((int64_t)blk * a.hkv + h) * ppb + p) * kF8Page;
             }
         }
-        const int cnt = (int)min((int64_t)32, end - g0);
-        for (int i = 0; i < cnt; ++i) {
+        // pages to convert: the set bits of `todo` (lane i: copy page g0 + i);
+        // each is copied whole into this warp's shared buffer with 16-byte
+        // asynchronous copies, the next one while the current one converts
+        unsigned todo = __ballot_sync(0xffffffffu, my_src != nullptr);
+        auto fetch = [&](int i, int bsel) {
             const unsigned char* src = reinterpret_cast<const unsigned char*>(
                 __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), i));
-            if (!src) continue;
+            const uint32_t dst = smem_addr(pbuf + bsel * kF8Page);
+            for (int c = lane; c < kF8Page / 16; c += 32)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * c), "l"(src + 16 * c)
+                             : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        int bsel = 0;
+        if (todo) fetch(__ffs(todo) - 1, 0);
+        while (todo) {
+            const int i = __ffs(todo) - 1;
+            todo &= todo - 1;
+            if (todo) {
+                fetch(__ffs(todo) - 1, bsel ^ 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            __syncwarp();  // every lane's copies of page i have landed
+            const unsigned char* src = pbuf + bsel * kF8Page;
             // copy page g0 + i = rows 16 p .. 16 p + 15 of copy block b, head h:
             // [b][h][block_size][128] has them at ((b * hkv + h) * ppb + p) * 16 rows
             const int64_t row0 = (g0 + i) * 16;
             __nv_bfloat16* kd = a.k_copy + row0 * kF8D;
             __nv_bfloat16* vd = a.v_copy + row0 * kF8D;
             const float* scales = reinterpret_cast<const float*>(src + kF8KsOff);
-            // K: lane takes chunk cc (16 dims) of tokens r = lane / 8 + 4 i
+            // K: lane takes chunk cc (16 dims) of tokens r = lane / 8 + 4 t
             const int cc = lane & 7;
-            uint4 kw[4];
-            float ks[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int r = (lane >> 3) + 4 * t;
-                kw[t] = *reinterpret_cast<const uint4*>(src + r * 128 + 16 * (cc ^ f8_swz(r)));
-                ks[t] = scales[r];
+                const uint4 kw = *reinterpret_cast<const uint4*>(src + r * 128 + 16 * (cc ^ f8_swz(r)));
+                const float ks = scales[r];
+                uint4 o0, o1;
+                expand4(kw.x, ks, o0.x, o0.y);
+                expand4(kw.y, ks, o0.z, o0.w);
+                expand4(kw.z, ks, o1.x, o1.y);
+                expand4(kw.w, ks, o1.z, o1.w);
+                *reinterpret_cast<uint4*>(kd + r * kF8D + 16 * cc) = o0;
+                *reinterpret_cast<uint4*>(kd + r * kF8D + 16 * cc + 8) = o1;
             }
             // V: lane takes dims 8 gv .. 8 gv + 7 of tokens 8 hv .. 8 hv + 7
             const int gv = lane >> 1, hv = lane & 1;
@@ -195,17 +225,6 @@ __global__ void __launch_bounds__(kExpandWarps * 32) prefill_fp8_expand(const Fp
             const float4 vs0 = *reinterpret_cast<const float4*>(src + kF8VsOff + 32 * hv);
             const float4 vs1 = *reinterpret_cast<const float4*>(src + kF8VsOff + 32 * hv + 16);
             const float vs[8] = {vs0.x, vs0.y, vs0.z, vs0.w, vs1.x, vs1.y, vs1.z, vs1.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int r = (lane >> 3) + 4 * t;
-                uint4 o0, o1;
-                expand4(kw[t].x, ks[t], o0.x, o0.y);
-                expand4(kw[t].y, ks[t], o0.z, o0.w);
-                expand4(kw[t].z, ks[t], o1.x, o1.y);
-                expand4(kw[t].w, ks[t], o1.z, o1.w);
-                *reinterpret_cast<uint4*>(kd + r * kF8D + 16 * cc) = o0;
-                *reinterpret_cast<uint4*>(kd + r * kF8D + 16 * cc + 8) = o1;
-            }
 #pragma unroll
             for (int tt = 0; tt < 8; ++tt) {
                 // token 8 hv + tt: byte tt % 4 of the low (tt < 4) or high word of each dim
@@ -220,6 +239,8 @@ __global__ void __launch_bounds__(kExpandWarps * 32) prefill_fp8_expand(const Fp
                 }
                 *reinterpret_cast<uint4*>(vd + (8 * hv + tt) * kF8D + 8 * gv) = make_uint4(o[0], o[1], o[2], o[3]);
             }
+            __syncwarp();  // buffer bsel is refilled two pages later
+            bsel ^= 1;
         }
     }
 }
@@ -284,10 +305,14 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
     prefill_fp8_plan<<<1, 1024, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
-    int per_sm = 0;  // one wave of resident CTAs (each warp walks a contiguous range of pages)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_fp8_expand, kExpandWarps * 32, 0);
+    constexpr int kExpandSmem = kExpandWarps * 2 * kF8Page;
+    static SmemLimit limit;
+    e = limit.ensure(reinterpret_cast<const void*>(prefill_fp8_expand), kExpandSmem);
     if (e != cudaSuccess) return cuda_status(e);
-    prefill_fp8_expand<<<num_sms() * std::max(1, per_sm), kExpandWarps * 32, 0, s>>>(a);
+    int per_sm = 0;  // one wave of resident CTAs (each warp walks a contiguous range of pages)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_fp8_expand, kExpandWarps * 32, kExpandSmem);
+    if (e != cudaSuccess) return cuda_status(e);
+    prefill_fp8_expand<<<num_sms() * std::max(1, per_sm), kExpandWarps * 32, kExpandSmem, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
     PrefillArgs b = pa;
