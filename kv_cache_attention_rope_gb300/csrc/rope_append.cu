@@ -116,7 +116,7 @@ __host__ __device__ constexpr ffc make_ffc(double d) { return {(float)d, (float)
 // with |k| <= 4 from a 5-entry float-float table of nested-radical values,
 // then Taylor series of the remainder x (|x| <= pi/32): terms above ~1e-6 in
 // float-float, the rest in float.  Absolute error about 2^-44.
-__device__ __noinline__ void accurate_twiddle(uint64_t u, const float4* sector, ff& c_out, ff& s_out)
+__device__ __forceinline__ void twiddle_core(uint64_t u, const float4* sector, ff& c_out, ff& s_out)
 {
     const uint32_t quad = (uint32_t)((u + (1ull << 61)) >> 62);  // nearest quarter turn
     const int64_t rs = (int64_t)(u - ((uint64_t)quad << 62));     // [-2^61, 2^61)
@@ -152,6 +152,21 @@ __device__ __noinline__ void accurate_twiddle(uint64_t u, const float4* sector, 
         case 2: c_out = ff_neg(ca); s_out = ff_neg(sa); break;
         default: c_out = sa; s_out = ff_neg(ca); break;
     }
+}
+
+__device__ __noinline__ void accurate_twiddle(uint64_t u, const float4* sector, ff& c_out, ff& s_out)
+{
+    twiddle_core(u, sector, c_out, s_out);
+}
+
+// Two angles at once: two independent dependency chains in one body, which
+// the scheduler interleaves (a lane's two twiddles one after the other were
+// the longest step of the ring's producer).
+__device__ __noinline__ void accurate_twiddle2(uint64_t u0, uint64_t u1, const float4* sector, ff& c0, ff& s0, ff& c1,
+                                               ff& s1)
+{
+    twiddle_core(u0, sector, c0, s0);
+    twiddle_core(u1, sector, c1, s1);
 }
 
 // Round-to-nearest-even of the float-float value y to bf16 bits.
@@ -649,9 +664,38 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
         // ================================ producer ================================
         const uint64_t policy = l2_evict_first_policy();
         int n = 0;  // tokens started by this CTA
+        // the token's cache slot (the same for every lane), looked up one token
+        // ahead: position and sequence at the top of the previous token's
+        // turn, the block-table entry after its twiddles, so that neither
+        // load's latency sits on this token's path
+        auto lookup = [&](int pos, int seq, long long& blk) -> bool {
+            bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
+            blk = -1;
+            if (ok) {
+                blk = a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size];
+                ok = blk >= 0 && blk < a.num_blocks;
+            }
+            return ok;
+        };
+        int pos_n = 0, seq_n = 0;
+        long long blk_n = -1;
+        bool ok_n = false;
+        if (blockIdx.x < (unsigned)a.num_tokens) {
+            pos_n = a.positions[blockIdx.x];
+            seq_n = a.seq_ids[blockIdx.x];
+            ok_n = lookup(pos_n, seq_n, blk_n);
+        }
         for (int t = blockIdx.x; t < a.num_tokens; t += gridDim.x, ++n) {
             const int s = n % stages, use = n / stages;
             unsigned char* st = smem + (size_t)s * stage_bytes;
+            const int pos = pos_n;
+            const bool ok = ok_n;
+            const long long blk = blk_n;
+            const int tn = t + gridDim.x;
+            if (tn < a.num_tokens) {
+                pos_n = a.positions[tn];
+                seq_n = a.seq_ids[tn];
+            }
             bool go = true;
             if (lane == 0) {
                 go = !*abort_flag;
@@ -669,15 +713,6 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (!go) break;
-            // the token's cache slot (the same for every lane)
-            const int pos = a.positions[t];
-            const int seq = a.seq_ids[t];
-            bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
-            long long blk = -1;
-            if (ok) {
-                blk = a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size];
-                ok = blk >= 0 && blk < a.num_blocks;
-            }
             if (lane == 0) {
                 if (!ok) record_error(a.status, KVATTN_ERR_BAD_INDEX);
                 PipeHeader* h = reinterpret_cast<PipeHeader*>(st);
@@ -686,12 +721,21 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
             }
             if (ok) {
                 float4* tw = reinterpret_cast<float4*>(st + 16);
-                for (int i = lane; i < kPairs; i += 32) {
-                    ff c, sn;
-                    accurate_twiddle((uint64_t)(uint32_t)pos * a.turns[i], sector, c, sn);
-                    tw[i] = make_float4(c.hi, c.lo, sn.hi, sn.lo);
+                if constexpr (kPairs == 64) {
+                    ff c0, s0, c1, s1;
+                    accurate_twiddle2((uint64_t)(uint32_t)pos * a.turns[lane], (uint64_t)(uint32_t)pos * a.turns[lane + 32],
+                                      sector, c0, s0, c1, s1);
+                    tw[lane] = make_float4(c0.hi, c0.lo, s0.hi, s0.lo);
+                    tw[lane + 32] = make_float4(c1.hi, c1.lo, s1.hi, s1.lo);
+                } else {
+                    for (int i = lane; i < kPairs; i += 32) {
+                        ff c, sn;
+                        accurate_twiddle((uint64_t)(uint32_t)pos * a.turns[i], sector, c, sn);
+                        tw[i] = make_float4(c.hi, c.lo, sn.hi, sn.lo);
+                    }
                 }
             }
+            if (tn < a.num_tokens) ok_n = lookup(pos_n, seq_n, blk_n);
             mbar_arrive(&full[s]);  // this lane's header/twiddle writes precede the arrival
         }
         // after an abort, let every armed copy land before the CTA can exit
