@@ -668,17 +668,14 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
         // ahead: position and sequence at the top of the previous token's
         // turn, the block-table entry after its twiddles, so that neither
         // load's latency sits on this token's path
-        auto lookup = [&](int pos, int seq, long long& blk) -> bool {
-            bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
-            blk = -1;
-            if (ok) {
-                blk = a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size];
-                ok = blk >= 0 && blk < a.num_blocks;
-            }
+        // (the entry is range-checked where it is used, so that its load is
+        // not waited for at the end of the previous token's turn)
+        auto lookup = [&](int pos, int seq, int& blk) -> bool {
+            const bool ok = pos >= 0 && seq >= 0 && seq < a.num_seqs && pos / a.block_size < a.max_blocks;
+            blk = ok ? a.block_table[(int64_t)seq * a.max_blocks + pos / a.block_size] : -1;
             return ok;
         };
-        int pos_n = 0, seq_n = 0;
-        long long blk_n = -1;
+        int pos_n = 0, seq_n = 0, blk_n = -1;
         bool ok_n = false;
         if (blockIdx.x < (unsigned)a.num_tokens) {
             pos_n = a.positions[blockIdx.x];
@@ -689,8 +686,8 @@ __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const
             const int s = n % stages, use = n / stages;
             unsigned char* st = smem + (size_t)s * stage_bytes;
             const int pos = pos_n;
-            const bool ok = ok_n;
             const long long blk = blk_n;
+            const bool ok = ok_n && blk >= 0 && blk < a.num_blocks;
             const int tn = t + gridDim.x;
             if (tn < a.num_tokens) {
                 pos_n = a.positions[tn];
