@@ -22,6 +22,7 @@ constexpr int kCopyThreads = 256;
 
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const __grid_constant__ CopyArgs a)
 {
+    pdl_wait();
     const int64_t vpb = a.block_bytes / 16;             // vectors per block-region
     const int64_t regions = 2 * (int64_t)a.layers;
     const int64_t total = (int64_t)a.n * regions * vpb;
@@ -48,7 +49,8 @@ kvattn_status launch_copy_blocks(const CopyArgs& a, cudaStream_t s)
     const int64_t total = (int64_t)a.n * 2 * a.layers * (a.block_bytes / 16);
     const int64_t want = (total + kCopyThreads - 1) / kCopyThreads;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, s>>>(a);
+    const cudaError_t e0 = launch_pdl(copy_blocks_kernel, dim3(grid), dim3(kCopyThreads), 0, s, a);
+    if (e0 != cudaSuccess) return cuda_status(e0);
     return cuda_status(cudaGetLastError());
 }
 

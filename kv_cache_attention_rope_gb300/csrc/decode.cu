@@ -48,9 +48,9 @@ constexpr int kMinPer = 4;  // fewest tiles in a CTA's range (flat mode)
 // residency the register and shared-memory budgets aim at: 3 CTAs per SM
 // (the tensor-core path keeps only rows 0..7 of its 16 x 8 fragments, which
 // fits it in 128 registers; at 3 CTAs it reads c4 at the HBM copy rate, at 2
-// CTAs with more registers it reached 90%).  The fp8 path is bound by its
-// instruction stream: 4 CTAs (96 registers) hide more latency (c4 0.664 ->
-// 0.645 ms).
+// CTAs with more registers it reached 90%).  The fp8 path runs 4 CTAs
+// (96 registers): its 4 KB pages need more producers issuing copies and more
+// consumer warps hiding MMA latency per byte than the 8 KB bf16 tiles.
 template <bool kMma, bool kFP8 = false>
 constexpr int ctas_per_sm() { return kFP8 ? 4 : 3; }
 
@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
                                                                 const __grid_constant__ PageMaps maps,
                                                                 const int stages)
 {
+    pdl_wait();
     using T = Traits<kBF16, kD, kGT>;
     static_assert(!kMma || (kBF16 && kD == 128 && kGT <= 8), "tensor-core path: bf16, D = 128, <= 8 heads");
     static_assert(!kFP8 || (kMma && !kRowBoxes), "fp8 cache: tensor-core path on 16-row pages");
@@ -966,6 +967,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kMma, kFP8>()) decode_sp
 template <bool kBF16, int kD>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ DecodeArgs a, const int gt)
 {
+    pdl_wait();
     const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (wid >= a.batch * a.hq) return;
     const int b = wid / a.hq, qh = wid - b * a.hq;
@@ -1036,13 +1038,11 @@ kvattn_status run(const DecodeArgs& a, cudaStream_t s)
         return KVATTN_ERR_CUDA;
     per_sm = std::max(1, per_sm);
     const int grid = num_sms() * per_sm;
-    kern<<<grid, kThreads, smem_bytes, s>>>(a, maps, stages);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem_bytes, s, a, maps, stages);
     if (e != cudaSuccess) return KVATTN_ERR_CUDA;
     if (a.splits > 1) {
         const int warps = a.batch * a.hq;
-        decode_combine_kernel<kBF16, kD><<<(warps + 3) / 4, 128, 0, s>>>(a, kGT);
-        e = cudaGetLastError();
+        e = launch_pdl(decode_combine_kernel<kBF16, kD>, dim3((warps + 3) / 4), dim3(128), 0, s, a, kGT);
     }
     return cuda_status(e);
 }

@@ -23,6 +23,28 @@ int* device_status_ptr();
 // One-line CUDA error mapping.
 inline kvattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA; }
 
+// Kernel launches with programmatic stream serialization: a kernel may be
+// scheduled while the kernel before it on the stream drains, which hides the
+// launch gap between the step's kernels.  Every kernel so launched starts
+// with pdl_wait(), which returns once the previous grid has completed and its
+// memory operations are visible, so stream order holds for every global
+// access (and a kernel launched without the attribute returns at once).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int num_sms();
 
 // Shared-memory figures of the current device (cached per device).
@@ -185,6 +207,9 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
                                  void* workspace, cudaStream_t s);
 
 // ---------------------------------------------------------------- device side
+
+// Waits for the grid launched before this one on the stream (see launch_pdl).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void record_error(int* status, int code)

@@ -226,6 +226,7 @@ template <int kHD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ Maps maps, const int n_qt)
 {
+    pdl_wait();
     using GE = Geo<kHD>;
     constexpr int kTileBytes = GE::kTileBytes, kPageBytes = GE::kPageBytes, kGroup = GE::kGroup;
     constexpr int kOffQ = GE::kOffQ, kOffK = GE::kOffK, kOffV = GE::kOffV;
@@ -853,8 +854,7 @@ kvattn_status launch_prefill_d(const PrefillArgs& a, cudaStream_t s)
     if (items <= 0) return KVATTN_OK;
     if (items > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
     const int64_t grid = std::min<int64_t>(items, num_sms());  // persistent: one CTA per SM
-    prefill_kernel<kHD><<<(unsigned)grid, kThreads, kSmem, s>>>(a, maps, n_qt);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(prefill_kernel<kHD>, dim3((unsigned)grid), dim3(kThreads), kSmem, s, a, maps, n_qt));
 }
 
 }  // namespace

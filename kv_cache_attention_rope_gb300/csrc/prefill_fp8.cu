@@ -69,6 +69,7 @@ __device__ __forceinline__ int chunk_blocks(const Fp8PrefillArgs& a, int c)
 
 __global__ void __launch_bounds__(1024) prefill_fp8_plan(const Fp8PrefillArgs a)
 {
+    pdl_wait();
     __shared__ int64_t wsum[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t carry = 0;
@@ -141,6 +142,7 @@ constexpr int kExpandWarps = 8;
 
 __global__ void __launch_bounds__(kExpandWarps * 32) prefill_fp8_expand(const Fp8PrefillArgs a)
 {
+    pdl_wait();
     extern __shared__ __align__(16) unsigned char bufs[];  // [kExpandWarps][2][kF8Page]
     const int lane = threadIdx.x & 31;
     unsigned char* pbuf = bufs + (threadIdx.x >> 5) * 2 * kF8Page;
@@ -302,8 +304,7 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
     a.k_copy = reinterpret_cast<__nv_bfloat16*>(ws + L.off_k);
     a.v_copy = reinterpret_cast<__nv_bfloat16*>(ws + L.off_v);
     a.status = pa.status;
-    prefill_fp8_plan<<<1, 1024, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prefill_fp8_plan, dim3(1), dim3(1024), 0, s, a);
     if (e != cudaSuccess) return cuda_status(e);
     constexpr int kExpandSmem = kExpandWarps * 2 * kF8Page;
     static SmemLimit limit;
@@ -312,8 +313,7 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
     int per_sm = 0;  // one wave of resident CTAs (each warp walks a contiguous range of pages)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_fp8_expand, kExpandWarps * 32, kExpandSmem);
     if (e != cudaSuccess) return cuda_status(e);
-    prefill_fp8_expand<<<num_sms() * std::max(1, per_sm), kExpandWarps * 32, kExpandSmem, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_fp8_expand, dim3(num_sms() * std::max(1, per_sm)), dim3(kExpandWarps * 32), kExpandSmem, s, a);
     if (e != cudaSuccess) return cuda_status(e);
     PrefillArgs b = pa;
     b.k_pool = a.k_copy;

@@ -273,6 +273,7 @@ __device__ __forceinline__ uint32_t rotate_bf16_word(uint32_t w, const Twiddle2&
 template <bool kBF16, int kD>
 __global__ void __launch_bounds__(128) rope_append_kernel(const __grid_constant__ RopeArgs a)
 {
+    pdl_wait();
     constexpr int kPairs = kD / 2;
     constexpr int kEPV = kBF16 ? 8 : 4;  // elements per 16-byte vector
     constexpr int kVPH = kD / kEPV;      // vectors per head
@@ -502,6 +503,7 @@ __device__ __forceinline__ unsigned char* fp8_page(const RopeArgs& a, int blk, i
 
 __global__ void __launch_bounds__(32, 24) append_v_fp8_kernel(const __grid_constant__ RopeArgs a)
 {
+    pdl_wait();
     __shared__ __align__(16) unsigned char tile[16 * 128];
     __shared__ float tsc[16];
     const int lane = threadIdx.x;
@@ -633,6 +635,7 @@ template <bool kBF16, int kD, bool kFP8>
 __global__ void __launch_bounds__(kPipeThreads, 8) rope_append_pipe_kernel(const __grid_constant__ RopeArgs a,
                                                                          const int stages, const int stage_bytes)
 {
+    pdl_wait();
     constexpr int kPairs = kD / 2;
     constexpr int kEPV = kBF16 ? 8 : 4;  // elements per 16-byte vector
     constexpr int kVPH = kD / kEPV;      // vectors per head
@@ -848,8 +851,7 @@ bool launch_pipe(const RopeArgs& a, cudaStream_t s, cudaError_t& err)
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, bytes);
     if (err != cudaSuccess) return true;
     const int grid = (int)std::min<int64_t>(a.num_tokens, (int64_t)num_sms() * std::max(1, per_sm));
-    kern<<<grid, kPipeThreads, bytes, s>>>(a, stages, (int)stage);
-    err = cudaGetLastError();
+    err = launch_pdl(kern, dim3(grid), dim3(kPipeThreads), bytes, s, a, stages, (int)stage);
     return true;
 }
 
@@ -858,8 +860,7 @@ kvattn_status launch_one(const RopeArgs& a, cudaStream_t s)
 {
     cudaError_t err = cudaSuccess;
     if (!launch_pipe<kBF16, kD, false>(a, s, err)) {
-        rope_append_kernel<kBF16, kD><<<a.num_tokens, 128, 0, s>>>(a);
-        err = cudaGetLastError();
+        err = launch_pdl(rope_append_kernel<kBF16, kD>, dim3(a.num_tokens), dim3(128), 0, s, a);
     }
     return cuda_status(err);
 }
@@ -884,8 +885,8 @@ kvattn_status launch_rope_append_fp8(const RopeArgs& a, cudaStream_t s)
     if (a.dtype == KVATTN_BF16 && a.d == 128) launched = launch_pipe<true, 128, true>(a, s, err);
     if (!launched) return KVATTN_ERR_UNSUPPORTED;
     if (err != cudaSuccess) return KVATTN_ERR_CUDA;
-    append_v_fp8_kernel<<<dim3((unsigned)((a.num_tokens + kVWin - 1) / kVWin), (unsigned)a.hkv), 32, 0, s>>>(a);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_pdl(append_v_fp8_kernel, dim3((unsigned)((a.num_tokens + kVWin - 1) / kVWin), (unsigned)a.hkv),
+                                  dim3(32), 0, s, a));
 }
 
 }  // namespace kvattn
