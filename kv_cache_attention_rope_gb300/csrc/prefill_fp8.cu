@@ -281,7 +281,10 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
                                  void* workspace, cudaStream_t s)
 {
     if (pa.num_chunks == 0 || pa.total_q == 0) return KVATTN_OK;
+    // launch_prefill's own refusals, checked before anything is launched
     if (L.nb * pa.hkv * pa.block_size >= ((int64_t)1 << 31)) return KVATTN_ERR_UNSUPPORTED;
+    if (pa.hq % pa.hkv || (pa.d != 128 && pa.d != 64)) return KVATTN_ERR_UNSUPPORTED;
+    if ((int64_t)pa.num_chunks * ((pa.max_q_len + 255) / 256) * pa.hq > 0x7fffffff) return KVATTN_ERR_UNSUPPORTED;
     unsigned char* ws = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(workspace) + kAlign - 1) / kAlign * kAlign);
     Fp8PrefillArgs a;
