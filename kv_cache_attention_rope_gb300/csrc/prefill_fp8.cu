@@ -307,14 +307,14 @@ kvattn_status launch_prefill_fp8(const PrefillArgs& pa, const void* pool, const 
     a.k_copy = reinterpret_cast<__nv_bfloat16*>(ws + L.off_k);
     a.v_copy = reinterpret_cast<__nv_bfloat16*>(ws + L.off_v);
     a.status = pa.status;
-    cudaError_t e = launch_pdl(prefill_fp8_plan, dim3(1), dim3(1024), 0, s, a);
-    if (e != cudaSuccess) return cuda_status(e);
     constexpr int kExpandSmem = kExpandWarps * 2 * kF8Page;
     static SmemLimit limit;
-    e = limit.ensure(reinterpret_cast<const void*>(prefill_fp8_expand), kExpandSmem);
+    cudaError_t e = limit.ensure(reinterpret_cast<const void*>(prefill_fp8_expand), kExpandSmem);
     if (e != cudaSuccess) return cuda_status(e);
     int per_sm = 0;  // one wave of resident CTAs (each warp walks a contiguous range of pages)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_fp8_expand, kExpandWarps * 32, kExpandSmem);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = launch_pdl(prefill_fp8_plan, dim3(1), dim3(1024), 0, s, a);
     if (e != cudaSuccess) return cuda_status(e);
     e = launch_pdl(prefill_fp8_expand, dim3(num_sms() * std::max(1, per_sm)), dim3(kExpandWarps * 32), kExpandSmem, s, a);
     if (e != cudaSuccess) return cuda_status(e);
